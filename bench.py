@@ -1,0 +1,350 @@
+#!/usr/bin/env python
+"""Ring-chunked exact attention, forward + backward, on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+the ring-chunked forward (online LSE merge) and the ring-chunked backward
+(row statistics, the recomputing backward kernel, dQ conversion) of the
+long-context video workload B=1, S=32760, H=24, D=128, P=8 ring chunks.
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  The throughput unit is TFLOP/s with the
+algorithmic flop count 14 * B * Hq * S^2 * D per step (4 forward, 10 for the
+backward that recomputes the probabilities).  N > 1 runs N independent
+replicas of the workload (the ring is emulated on one GPU; there is no
+data-path collective), launched by torchrun.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from seeded_inputs import VIDEO_S32760_P8, AttnShape, attn_inputs, exchange_input  # noqa: E402
+
+METRIC = "fwd+bwd attention TFLOP/s at 1 GB300 (ring P chunks), % of dense bf16 peak"
+UNIT = "TFLOP/s"
+WORKLOAD = VIDEO_S32760_P8
+WORKLOAD_NAME = "video-DiT long context MHA fwd+bwd, B=1 S=32760 H=24 D=128, P=8 ring chunks (8 x 4095)"
+L2_NOTE = "inputs larger than L2 (q/k/v/dout 805 MB vs 126.5 MB L2); no flush"
+
+# dram traffic per launch of the backward kernel from one ncu capture (see
+# profiles/); valid only while the kernel source is the one it was taken on.
+NCU_BWD = {"bytes_per_launch": None, "source_sha256": None}
+
+
+def flops_fwd(sh: AttnShape) -> float:
+    return 4.0 * sh.B * sh.Hq * sh.S * sh.S * sh.D
+
+
+def flops_bwd(sh: AttnShape) -> float:
+    return 10.0 * sh.B * sh.Hq * sh.S * sh.S * sh.D
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"bf16": pk["bf16_tflops"], "bf16_sustained": pk["bf16_tflops_sustained"],
+                "hbm": pk["hbm_gbs"], "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.proc = None
+        self.dev = device_index
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.dev)], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_sample(S_sample: int):
+    """Times the fp64 oracle (forward + analytic backward) on head 0 of the
+    workload truncated to its first S_sample rows; returns (TFLOP/s, seconds)."""
+    import oracle
+
+    sh = AttnShape(B=1, S=S_sample, Hq=1, Hkv=1, D=WORKLOAD.D, P=1)
+    q, k, v, do = attn_inputs(sh, seed=777)
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.attn_fwd(q, k, v)
+    oracle.attn_bwd(q, k, v, do)
+    dt = time.perf_counter() - t0
+    return 14.0 * S_sample * S_sample * sh.D / dt / 1e12, dt
+
+
+def run_reference(args, world, rank):
+    """The oracle, as it stands, on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    S_step = 4095  # one ring chunk of head 0 per step
+    for _ in range(args.warmup):
+        cpu_sample(S_step)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        cpu_sample(S_step)
+    dt = time.perf_counter() - t0
+    val = args.steps * 14.0 * S_step * S_step * WORKLOAD.D / dt / 1e12
+    cores = os.cpu_count()
+    sample = (f"fp64 oracle forward + analytic backward of head 0 of the workload truncated to "
+              f"its first ring chunk (S={S_step}, D={WORKLOAD.D}) per step")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_dict(),
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def config_dict():
+    sh = WORKLOAD
+    return {"workload": WORKLOAD_NAME, "B": sh.B, "S": sh.S, "Hq": sh.Hq, "Hkv": sh.Hkv, "D": sh.D,
+            "P": sh.P, "layout": sh.layout, "causal": False, "l2": L2_NOTE}
+
+
+def source_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, local = dist_setup()
+
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import context_attention_fwd_gb300 as ctx
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    ctx.load_library(build_if_missing=True)
+    sh = WORKLOAD
+    peaks = load_peaks()
+
+    q_h, k_h, v_h, do_h = attn_inputs(sh)
+    q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+    out = torch.empty_like(q)
+    lse = torch.empty(sh.B, sh.Hq, sh.S, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(ctx.workspace_size(sh.B, sh.S, sh.Hq, sh.Hkv, sh.D, sh.P), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ctx.attn_fwd(q, k, v, sh.P, out=out, lse=lse)
+        ctx.attn_bwd(q, k, v, out, lse, do, sh.P, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    if ctx.device_status() != 0:
+        raise RuntimeError("device-side wait timed out during warm-up")
+
+    # ------------------------------------------------ device-resident timing
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ctx.profile_enable(True)
+    with ClockSampler(local) as clk:
+        barrier()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        barrier()
+    ctx.profile_enable(False)
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = t.item()
+    if ctx.device_status() != 0:
+        raise RuntimeError("device-side wait timed out during the timed region")
+    flops_step = flops_fwd(sh) + flops_bwd(sh)
+    value = world * flops_step * args.steps / (ms / 1e3) / 1e12
+    bwd_ms, bwd_n = ctx.profile_read("bwd")
+    fwd_ms, fwd_n = ctx.profile_read("fwd")
+    bwd_avg, fwd_avg = bwd_ms / max(bwd_n, 1), fwd_ms / max(fwd_n, 1)
+    bwd_tf = flops_bwd(sh) / (bwd_avg / 1e3) / 1e12
+    fwd_tf = flops_fwd(sh) / (fwd_avg / 1e3) / 1e12
+    bwd_src = os.path.join(ROOT, "context_attention_fwd_gb300", "csrc", "attn_bwd.cu")
+    traffic = NCU_BWD["bytes_per_launch"] if NCU_BWD["source_sha256"] == source_sha(bwd_src) else None
+    peak = peaks["bf16_sustained"]
+    clocks = clk.summary()
+
+    # ------------------------------------------------ end to end, host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.contiguous().pin_memory()
+        hq, hk, hv, hdo = (pin(t) for t in (q_h, k_h, v_h, do_h))
+        hout, hdq, hdk, hdv = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                               for t in (q_h, q_h, k_h, k_h))
+        hlse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+        def e2e_step():
+            for d, h in ((q, hq), (k, hk), (v, hv), (do, hdo)):
+                d.copy_(h, non_blocking=True)
+            step()
+            for h, d in ((hout, out), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+                h.copy_(d, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ems = t.item()
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+        d2h = sum(t.numel() * t.element_size() for t in (hout, hlse, hdq, hdk, hdv))
+        e2e = {"value": world * flops_step * args.steps / (ems / 1e3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems / args.steps}
+
+    # ------------------------------------------------ the exchange (HBM bound)
+    xq = exchange_input(1, 65536, 32, 128, seed=5).to(dev)
+    y = ctx.seq_head_exchange(xq, 4, 2, 0, "bshd")
+    back = ctx.seq_head_exchange(y, 4, 2, 1, "bshd", S=65536, B=1, H=32)
+    barrier()
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 10
+    x0.record(stream)
+    for _ in range(reps):
+        ctx.seq_head_exchange(xq, 4, 2, 0, "bshd", y=y)
+        ctx.seq_head_exchange(y, 4, 2, 1, "bshd", y=back, S=65536, B=1, H=32)
+    x1.record(stream)
+    barrier()
+    xms = x0.elapsed_time(x1) / (2 * reps)
+    xbytes = 2 * xq.numel() * xq.element_size()
+    x_gbs = xbytes / (xms / 1e3) / 1e9
+    del xq, y, back
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_dict(),
+        "pct_of_peak": {"burst": 100.0 * value / world / peaks["bf16"],
+                        "sustained": 100.0 * value / world / peaks["bf16_sustained"],
+                        "peaks_source": peaks["source"]},
+        "clocks": clocks,
+        "gpu_launches": 4 * args.steps,
+        "roofline": {"kernel": "attn_bwd_kernel<128>", "bound": "tensor", "achieved": bwd_tf,
+                     "peak": peak, "unit": "TFLOP/s", "frac": bwd_tf / peak, "traffic": traffic,
+                     "peak_kind": f"bf16 dense, sustained ({peaks['source']})",
+                     "launches": bwd_n, "avg_ms": bwd_avg},
+        "roofline_fwd": {"kernel": "attn_fwd_kernel<128>", "bound": "tensor", "achieved": fwd_tf,
+                         "peak": peak, "unit": "TFLOP/s", "frac": fwd_tf / peak,
+                         "launches": fwd_n, "avg_ms": fwd_avg},
+        "exchange": {"shape": [1, 65536, 32, 128], "ring": 4, "ulysses": 2, "bound": "hbm",
+                     "achieved": x_gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                     "frac": x_gbs / peaks["hbm"], "ms": xms},
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        val, secs = cpu_sample(8190)
+        line["cpu_baseline"] = {
+            "value": val, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": ("fp64 oracle forward + analytic backward of head 0 of the workload truncated "
+                       f"to its first two ring chunks (S=8190, D=128), {secs:.1f} s")}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,442 @@
+// attn_bwd.cu -- ring-chunked attention backward for sm_103a.
+//
+// One CTA owns one 128-row KV tile of ring chunk c for one (batch, kv head).
+// It keeps K_c and V_c resident in shared memory and visits the query
+// chunks in ring order r = (c + i) mod P, i = 0..P-1 (at iteration i query
+// chunk r met KV chunk (r - i) mod P = c in the forward), for every query
+// head of its GQA group.  For every (query tile, this KV tile) pair the
+// probabilities are recomputed against this chunk's own K_c with the merged
+// log-sum-exp of the forward -- the per-iteration K/V the backward must see
+// (diffusers issue #14265, "Expected behavior"; recompute instead of saving
+// per-iteration tensors) -- so the stale iteration-0 K/V defect of
+// "Root cause" cannot occur: the only K/V in the CTA is K_c, V_c.
+//
+// Per query tile (all matrices are per (b, h), fp32 accumulation):
+//   S^T  = K_c Q^T                      TMEM[S]     (M = kv, N = q, K = D)
+//   P^T  = exp2(S^T * scale*log2e - lse*log2e)      -> bf16 into TMEM[S]
+//   dP^T = V_c dO^T                     TMEM[dP]
+//   dS^T = P^T o (dP^T - delta)         -> bf16 into shared memory
+//   dV  += P^T dO                       TMEM[dV]    (A from TMEM)
+//   dK  += dS^T Q                       TMEM[dK]    (A = dS^T, K-major)
+//   dQ   = dS K_c                       TMEM[dP]    (A = dS, MN-major view of dS^T)
+// dQ tiles are added into an fp32 accumulator in global memory (vector
+// reductions); dK, dV stay in TMEM for the whole CTA and are written once.
+//
+// Warp roles (320 threads):
+//   warp 0      TMA producer (K, V once; Q, dO, lse, delta per query tile, 2 stages)
+//   warp 1      TMEM owner and MMA issuer
+//   warps 2..5  P / dS math, one KV row per thread; dV epilogue
+//   warps 6..9  dQ drain (one query row per thread); dK epilogue
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ctxattn {
+namespace {
+
+template <int D>
+struct BwdLayout {
+    static constexpr int NBOX = D / 64;
+    static constexpr uint32_t BOX = kTile * 128;     // 128 rows x 128 bytes
+    static constexpr uint32_t TILE = kTile * D * 2;  // 128 x D bf16
+    static constexpr uint32_t DS_TILE = kTile * 128 * 2;
+    static constexpr uint32_t OFF_K = 0;
+    static constexpr uint32_t OFF_V = OFF_K + TILE;
+    static constexpr uint32_t OFF_Q = OFF_V + TILE;          // 2 stages
+    static constexpr uint32_t OFF_DO = OFF_Q + 2 * TILE;     // 2 stages
+    static constexpr uint32_t OFF_DS = OFF_DO + 2 * TILE;
+    static constexpr uint32_t OFF_STAT = OFF_DS + DS_TILE;   // 2 stages x (lse2[128], delta[128])
+    static constexpr uint32_t OFF_BARS = OFF_STAT + 2 * 1024;
+    static constexpr uint32_t SMEM = OFF_BARS + 256;
+    static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 384, TM_COLS = 512;
+};
+
+struct BwdBars {
+    uint64_t kv_full;
+    uint64_t q_full[2], q_empty[2];
+    uint64_t s_full, dp_full, p_ready, ds_ready, ds_free;
+    uint64_t dq_full, dq_drained;
+    uint64_t final_mma;
+    uint64_t drain;
+    uint32_t tmem_slot;
+    int abort_flag;
+};
+
+constexpr int kMathThreads = 128;
+
+__device__ __forceinline__ int pick3(int o, int s, int h, int b) {
+    return o == 0 ? s : (o == 1 ? h : b);
+}
+__device__ __forceinline__ void tma_tile(const TmaMap& m, uint32_t dst, uint32_t bar, int d0, int s,
+                                         int h, int b) {
+    tma_load_4d(dst, &m.map, bar, d0, pick3(m.ord[0], s, h, b), pick3(m.ord[1], s, h, b),
+                pick3(m.ord[2], s, h, b));
+}
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > limit_ns) break;
+}
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
+// Iteration order over the query tiles one CTA visits: for every query head
+// of the group, the ring iterations i = 0..P-1 (query chunk (c + i) mod P),
+// and the 128-row tiles of that chunk.
+struct QTileIter {
+    int h, t, it, r;
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
+    using L = BwdLayout<D>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    BwdBars& bars = *reinterpret_cast<BwdBars*>(smem + L::OFF_BARS);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sK = sbase + L::OFF_K, sV = sbase + L::OFF_V, sQ = sbase + L::OFF_Q,
+                   sDO = sbase + L::OFF_DO, sDS = sbase + L::OFF_DS;
+    const float* stat_base = reinterpret_cast<const float*>(smem + L::OFF_STAT);
+    const int warp = warp_id(), lane = lane_id();
+    const int kt = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+    const ChunkTable& ct = p.ct;
+    const int P = ct.P;
+    const int c = chunk_of_tile(ct, kt);
+    const int kv_start = ct.off[c] + (kt - ct.tile_off[c]) * kTile;
+    const int kv_len = min(kTile, ct.off[c + 1] - kv_start);
+    const int G = p.group;
+    const int n_q = G * ct.ntiles;
+    const WaitCtx wc{&bars.abort_flag, p.status, p.timeout_ns};
+
+    if (sbase & 1023u) {  // the swizzled tiles need 1024-byte alignment
+        if (threadIdx.x == 0) atomicExch(p.status, 2);
+        return;
+    }
+    if (threadIdx.x == 0) {
+        bars.abort_flag = 0;
+        mbar_init(smem_u32(&bars.kv_full), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&bars.q_full[i]), 1);
+            mbar_init(smem_u32(&bars.q_empty[i]), 1 + 4);  // MMA commit + one per math warp
+        }
+        mbar_init(smem_u32(&bars.s_full), 1);
+        mbar_init(smem_u32(&bars.dp_full), 1);
+        mbar_init(smem_u32(&bars.p_ready), kMathThreads);
+        mbar_init(smem_u32(&bars.ds_ready), kMathThreads);
+        mbar_init(smem_u32(&bars.ds_free), 1);
+        mbar_init(smem_u32(&bars.dq_full), 1);
+        mbar_init(smem_u32(&bars.dq_drained), kMathThreads);
+        mbar_init(smem_u32(&bars.final_mma), 1);
+        mbar_init(smem_u32(&bars.drain), 1);
+        mbar_fence_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&bars.tmem_slot), L::TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars.tmem_slot;
+
+    // advance a query-tile iterator
+    auto next = [&](QTileIter& q) {
+        ++q.t;
+        if (q.t == ct.tile_off[q.r + 1]) {
+            ++q.it;
+            if (q.it == P) {
+                q.it = 0;
+                ++q.h;
+            }
+            q.r = (c + q.it) % P;
+            q.t = ct.tile_off[q.r];
+        }
+    };
+    QTileIter q0;
+    q0.h = hk * G;
+    q0.it = 0;
+    q0.r = c;
+    q0.t = ct.tile_off[c];
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tq.map);
+            tma_prefetch_desc(&p.tk.map);
+            tma_prefetch_desc(&p.tv.map);
+            tma_prefetch_desc(&p.tdo.map);
+            const uint32_t kvf = smem_u32(&bars.kv_full);
+            mbar_arrive_expect_tx(kvf, 2 * L::TILE);
+            for (int bx = 0; bx < L::NBOX; ++bx) {
+                tma_tile(p.tk, sK + bx * L::BOX, kvf, bx * 64, kv_start, hk, b);
+                tma_tile(p.tv, sV + bx * L::BOX, kvf, bx * 64, kv_start, hk, b);
+            }
+            QTileIter q = q0;
+            int last_ph[2] = {-1, -1};
+            bool ok = true;
+            for (int i = 0; i < n_q; ++i, next(q)) {
+                const int st = i & 1, ph = (i >> 1) & 1;
+                if (!(ok = mbar_wait(smem_u32(&bars.q_empty[st]), ph ^ 1, wc))) break;
+                const uint32_t qf = smem_u32(&bars.q_full[st]);
+                mbar_arrive_expect_tx(qf, 2 * L::TILE + 1024);
+                const int q_start = ct.off[q.r] + (q.t - ct.tile_off[q.r]) * kTile;
+                for (int bx = 0; bx < L::NBOX; ++bx) {
+                    tma_tile(p.tq, sQ + st * L::TILE + bx * L::BOX, qf, bx * 64, q_start, q.h, b);
+                    tma_tile(p.tdo, sDO + st * L::TILE + bx * L::BOX, qf, bx * 64, q_start, q.h, b);
+                }
+                const size_t slot = ((size_t)(b * p.Hq + q.h) * ct.ntiles + q.t) * kTile;
+                const uint32_t sst = sbase + L::OFF_STAT + st * 1024;
+                bulk_load(sst, p.lse2 + slot, 512, qf);
+                bulk_load(sst + 512, p.delta + slot, 512, qf);
+                last_ph[st] = ph;
+            }
+            if (!ok) {
+                drain_wait(kvf, 0, p.timeout_ns);
+                for (int st = 0; st < 2; ++st)
+                    if (last_ph[st] >= 0) drain_wait(smem_u32(&bars.q_full[st]), last_ph[st], p.timeout_ns);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id_st = idesc_bf16_f32(128, 128, false, false);  // K-major A and B
+            constexpr uint32_t id_dv = idesc_bf16_f32(128, D, false, true);     // A TMEM, B MN-major
+            constexpr uint32_t id_dk = idesc_bf16_f32(128, D, false, true);     // A K-major smem, B MN-major
+            constexpr uint32_t id_dq = idesc_bf16_f32(128, D, true, true);      // A MN-major, B MN-major
+            bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, wc);
+            for (int i = 0; i < n_q && ok; ++i) {
+                const int st = i & 1, ph = (i >> 1) & 1;
+                const uint32_t sQs = sQ + st * L::TILE, sDOs = sDO + st * L::TILE;
+                if (!(ok = mbar_wait(smem_u32(&bars.q_full[st]), ph, wc))) break;
+                tc_fence_after();
+                // S^T = K Q^T
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t koff = (kk >> 2) * L::BOX + (kk & 3) * 32;
+                    mma_ss(tmem + L::TM_S, sdesc_sw128(sK + koff, 16, 1024),
+                           sdesc_sw128(sQs + koff, 16, 1024), id_st, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(smem_u32(&bars.s_full));
+                // dP^T = V dO^T, into the columns the previous dQ occupied
+                if (i > 0 && !(ok = mbar_wait(smem_u32(&bars.dq_drained), (i - 1) & 1, wc))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t koff = (kk >> 2) * L::BOX + (kk & 3) * 32;
+                    mma_ss(tmem + L::TM_DP, sdesc_sw128(sV + koff, 16, 1024),
+                           sdesc_sw128(sDOs + koff, 16, 1024), id_st, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(smem_u32(&bars.dp_full));
+                // dV += P^T dO
+                if (!(ok = mbar_wait(smem_u32(&bars.p_ready), i & 1, wc))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    mma_ts(tmem + L::TM_DV, tmem + L::TM_S + kk * 8,
+                           sdesc_sw128(sDOs + kk * 2048, L::BOX, 1024), id_dv,
+                           (i > 0 || kk > 0) ? 1u : 0u);
+                // dK += dS^T Q ; dQ = dS K
+                if (!(ok = mbar_wait(smem_u32(&bars.ds_ready), i & 1, wc))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk) {
+                    const uint32_t koff = (kk >> 2) * L::BOX + (kk & 3) * 32;
+                    mma_ss(tmem + L::TM_DK, sdesc_sw128(sDS + koff, 16, 1024),
+                           sdesc_sw128(sQs + kk * 2048, L::BOX, 1024), id_dk,
+                           (i > 0 || kk > 0) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    mma_ss(tmem + L::TM_DP, sdesc_sw128(sDS + kk * 2048, L::BOX, 1024),
+                           sdesc_sw128(sK + kk * 2048, L::BOX, 1024), id_dq, kk > 0 ? 1u : 0u);
+                mma_commit(smem_u32(&bars.dq_full));
+                mma_commit(smem_u32(&bars.ds_free));
+                mma_commit(smem_u32(&bars.q_empty[st]));
+            }
+            mma_commit(smem_u32(&bars.final_mma));
+            mma_commit(smem_u32(&bars.drain));
+            drain_wait(smem_u32(&bars.drain), 0, p.timeout_ns);
+        }
+    } else if (warp < 6) {
+        // ---------------------------------------------------------- P / dS math
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;  // KV row of this thread
+        const uint32_t taddr = tmem + (uint32_t(quarter * 32) << 16);
+        const float sc = p.scale_log2;
+        const bool row_valid = row < kv_len;
+        bool ok = true;
+        for (int i = 0; i < n_q; ++i) {
+            const int st = i & 1, ph = (i >> 1) & 1;
+            const float* lse2 = stat_base + st * 256;
+            const float* delta = lse2 + 128;
+            if (!(ok = mbar_wait(smem_u32(&bars.q_full[st]), ph, wc))) break;
+            if (!(ok = mbar_wait(smem_u32(&bars.s_full), i & 1, wc))) break;
+            tc_fence_after();
+            uint32_t pr[128];
+            tmem_ld32(taddr + L::TM_S + 0, pr);
+            tmem_ld32(taddr + L::TM_S + 32, pr + 32);
+            tmem_ld32(taddr + L::TM_S + 64, pr + 64);
+            tmem_ld32(taddr + L::TM_S + 96, pr + 96);
+            tmem_ld_wait();
+            reg_fence32(pr);
+            reg_fence32(pr + 32);
+            reg_fence32(pr + 64);
+            reg_fence32(pr + 96);
+            // P^T (fp32 kept in pr); padded query columns have lse2 = +inf -> 0
+#pragma unroll
+            for (int k = 0; k < 128; ++k) {
+                const float pv = ex2(fmaf(__uint_as_float(pr[k]), sc, -lse2[k]));
+                pr[k] = __float_as_uint(row_valid ? pv : 0.f);
+            }
+            {
+                uint32_t pk[32];
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        pk[k] = pack_bf16x2(__uint_as_float(pr[64 * half + 2 * k]),
+                                            __uint_as_float(pr[64 * half + 2 * k + 1]));
+                    tmem_st32(taddr + L::TM_S + 32 * half, pk);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.p_ready));
+            // dS^T = P^T o (dP^T - delta), to shared memory as bf16
+            if (!(ok = mbar_wait(smem_u32(&bars.dp_full), i & 1, wc))) break;
+            if (i > 0 && !(ok = mbar_wait(smem_u32(&bars.ds_free), (i - 1) & 1, wc))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t dp[32];
+                tmem_ld32(taddr + L::TM_DP + cc * 32, dp);
+                tmem_ld_wait();
+                reg_fence32(dp);
+                uint32_t w[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int q0i = cc * 32 + 2 * k;
+                    const float d0 = __uint_as_float(pr[q0i]) * (__uint_as_float(dp[2 * k]) - delta[q0i]);
+                    const float d1 =
+                        __uint_as_float(pr[q0i + 1]) * (__uint_as_float(dp[2 * k + 1]) - delta[q0i + 1]);
+                    w[k] = pack_bf16x2(d0, d1);
+                }
+                // 32 query columns = four 16-byte chunks of the 128-byte swizzled row
+                const uint32_t box = sDS + (cc >> 1) * L::BOX;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const uint32_t addr = box + sw128_offset(row, (cc & 1) * 4 + m);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[4 * m]),
+                                 "r"(w[4 * m + 1]), "r"(w[4 * m + 2]), "r"(w[4 * m + 3])
+                                 : "memory");
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.ds_ready));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars.q_empty[st]));
+        }
+        // ---------------------------------------------------------- dV epilogue
+        if (ok && mbar_wait(smem_u32(&bars.final_mma), 0, wc)) {
+            tc_fence_after();
+            __nv_bfloat16* dst =
+                p.dv + (int64_t)b * p.k_sb + (int64_t)(kv_start + row) * p.k_ss + (int64_t)hk * p.k_sh;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t o[32];
+                tmem_ld32(taddr + L::TM_DV + cc * 32, o);
+                tmem_ld_wait();
+                reg_fence32(o);
+                if (row_valid) {
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        d4[k] = make_uint4(
+                            pack_bf16x2(__uint_as_float(o[8 * k + 0]), __uint_as_float(o[8 * k + 1])),
+                            pack_bf16x2(__uint_as_float(o[8 * k + 2]), __uint_as_float(o[8 * k + 3])),
+                            pack_bf16x2(__uint_as_float(o[8 * k + 4]), __uint_as_float(o[8 * k + 5])),
+                            pack_bf16x2(__uint_as_float(o[8 * k + 6]), __uint_as_float(o[8 * k + 7])));
+                }
+            }
+        }
+    } else {
+        // ---------------------------------------------------------- dQ drain
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;  // query row of the current tile
+        const uint32_t taddr = tmem + (uint32_t(quarter * 32) << 16);
+        QTileIter q = q0;
+        bool ok = true;
+        for (int i = 0; i < n_q; ++i, next(q)) {
+            if (!(ok = mbar_wait(smem_u32(&bars.dq_full), i & 1, wc))) break;
+            tc_fence_after();
+            uint32_t v[D];
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(taddr + L::TM_DP + cc * 32, v + cc * 32);
+            tmem_ld_wait();
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) reg_fence32(v + cc * 32);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.dq_drained));
+            // tile-major accumulator: [(b,h,t)][D/4][128 rows][4]
+            float* tile = p.dq_acc + ((size_t)(b * p.Hq + q.h) * ct.ntiles + q.t) * (size_t)(kTile * D);
+#pragma unroll
+            for (int g = 0; g < D / 4; ++g)
+                red_add_v4(tile + ((size_t)g * kTile + row) * 4, __uint_as_float(v[4 * g]),
+                           __uint_as_float(v[4 * g + 1]), __uint_as_float(v[4 * g + 2]),
+                           __uint_as_float(v[4 * g + 3]));
+        }
+        // ---------------------------------------------------------- dK epilogue
+        if (ok && mbar_wait(smem_u32(&bars.final_mma), 0, wc)) {
+            tc_fence_after();
+            const bool row_valid = row < kv_len;
+            __nv_bfloat16* dst =
+                p.dk + (int64_t)b * p.k_sb + (int64_t)(kv_start + row) * p.k_ss + (int64_t)hk * p.k_sh;
+            const float scale = p.scale;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t o[32];
+                tmem_ld32(taddr + L::TM_DK + cc * 32, o);
+                tmem_ld_wait();
+                reg_fence32(o);
+                if (row_valid) {
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        d4[k] = make_uint4(
+                            pack_bf16x2(__uint_as_float(o[8 * k + 0]) * scale, __uint_as_float(o[8 * k + 1]) * scale),
+                            pack_bf16x2(__uint_as_float(o[8 * k + 2]) * scale, __uint_as_float(o[8 * k + 3]) * scale),
+                            pack_bf16x2(__uint_as_float(o[8 * k + 4]) * scale, __uint_as_float(o[8 * k + 5]) * scale),
+                            pack_bf16x2(__uint_as_float(o[8 * k + 6]) * scale, __uint_as_float(o[8 * k + 7]) * scale));
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, L::TM_COLS);
+}
+
+template <int D>
+int launch_bwd_d(const BwdParams& p, cudaStream_t s) {
+    using L = BwdLayout<D>;
+    if (cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::SMEM) != cudaSuccess)
+        return 4;
+    dim3 grid(p.ct.ntiles, p.Hkv, p.B);
+    attn_bwd_kernel<D><<<grid, 320, L::SMEM, s>>>(p);
+    return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+}  // namespace
+
+int launch_attn_bwd(const BwdParams& p, int D, cudaStream_t s) {
+    if (D == 64) return launch_bwd_d<64>(p, s);
+    if (D == 128) return launch_bwd_d<128>(p, s);
+    return 2;
+}
+
+}  // namespace ctxattn

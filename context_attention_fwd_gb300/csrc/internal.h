@@ -1,0 +1,69 @@
+// internal.h -- parameter blocks and launchers shared by the translation
+// units of the library (not part of the C ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tmap.h"
+
+namespace ctxattn {
+
+constexpr int kMaxChunks = 64;
+constexpr int kTile = 128;  // rows of a query or key/value tile
+
+// Ring chunk table: chunk c holds rows [off[c], off[c+1]) and 128-row tiles
+// [tile_off[c], tile_off[c+1]) of the tile numbering (tiles never straddle
+// a chunk boundary; a chunk's last tile may be partial).
+struct ChunkTable {
+    int P;
+    int ntiles;  // tile_off[P]
+    int off[kMaxChunks + 1];
+    int tile_off[kMaxChunks + 1];
+};
+
+__host__ __device__ inline int chunk_of_tile(const ChunkTable& ct, int t) {
+    int c = 0;
+    while (c + 1 < ct.P && ct.tile_off[c + 1] <= t) ++c;
+    return c;
+}
+
+struct FwdParams {
+    TmaMap tq, tk, tv;
+    ChunkTable ct;
+    int B, S, Hq, Hkv, group;
+    float scale;       // softmax scale
+    float scale_log2;  // scale * log2(e)
+    __nv_bfloat16* out;
+    int64_t o_sb, o_ss, o_sh;
+    float* lse;  // [B,Hq,S]
+    // materialised partials (nullptr unless requested):
+    // part_o [P][B][Hq][S][D] fp32 normalised, part_lse [P][B][Hq][S] natural log
+    float* part_o;
+    float* part_lse;
+    int* status;
+    uint64_t timeout_ns;
+};
+
+struct BwdParams {
+    TmaMap tq, tk, tv, tdo;
+    ChunkTable ct;
+    int B, S, Hq, Hkv, group;
+    float scale, scale_log2;
+    // per-row statistics in tile-major order [B][Hq][ntiles][128]:
+    const float* lse2;   // lse * log2(e)
+    const float* delta;  // rowsum(dO o O)
+    // fp32 dQ accumulator, tile-major [B][Hq][ntiles][D/4][128][4], zeroed
+    float* dq_acc;
+    __nv_bfloat16* dk;
+    __nv_bfloat16* dv;
+    int64_t k_sb, k_ss, k_sh;  // strides of dk/dv
+    int* status;
+    uint64_t timeout_ns;
+};
+
+int launch_attn_fwd(const FwdParams& p, int D, cudaStream_t s);
+int launch_attn_bwd(const BwdParams& p, int D, cudaStream_t s);
+
+}  // namespace ctxattn

@@ -1,0 +1,164 @@
+/*
+ * ctx_attn.h -- C ABI of the ring-chunked exact attention library (sm_103a).
+ *
+ * What it computes.  Exact softmax attention over a sequence cut into P
+ * chunks on the ring schedule of context parallelism, emulated on one GPU:
+ * query chunk r meets KV chunk (r - i) mod P at ring iteration i, each
+ * iteration yields a partial (O_i, LSE_i) and the partials are merged by LSE
+ * weighting (diffusers issue #14265 "Ring attention backward uses stale
+ * iteration-0 KV from ctx.saved_tensors ...", sections "Root cause" and
+ * "How it surfaces per backend": the ring needs the LSE to merge partial
+ * results).  The backward recomputes the probabilities of every (query
+ * chunk, KV chunk) pair against that pair's own KV chunk, which is what the
+ * same issue's "Expected behavior" asks for; the stale-K/V defect it reports
+ * cannot occur.  The Ulysses sequence<->head exchange (DeepSpeed PR #8491
+ * "[bugfix] _DimZeroAllToAll silently fails to send grads under
+ * torch.compile"; DeepSpeed issue #7842 "[BUG] DistributedAttention produces
+ * numerically incorrect results ...") is an on-device permutation.
+ *
+ * Conventions common to every entry point.
+ *  - Device memory (inputs, outputs, workspace) is allocated and owned by the
+ *    caller.  The library allocates nothing and frees nothing.
+ *  - Work is enqueued on the caller's stream and is asynchronous; no entry
+ *    point synchronises except ctx_get_device_status.
+ *  - Arguments are validated before anything is launched; an invalid call
+ *    returns an error code and writes nothing (never a silent wrong result).
+ *  - Element type: bf16 for q, k, v, out, dout, dq, dk, dv; fp32 for lse.
+ *  - Head dimension D is 64 or 128 (others: CTX_ERR_UNSUPPORTED).
+ *  - Chunks: chunk_offsets == NULL means numpy-array_split chunking (the first
+ *    S mod P chunks are one row longer); otherwise a host array of P+1
+ *    strictly increasing offsets from 0 to S.  Empty chunks are rejected.
+ *    Chunks need not be multiples of the 128-row tile: tails are masked.
+ *  - GQA: Hq must be a multiple of Hkv; query head h uses kv head
+ *    h / (Hq / Hkv) (issue #14265, "How it surfaces": the heads of K/V must
+ *    divide the heads of Q).
+ *  - Scale: scale <= 0 selects 1/sqrt(D).
+ *  - Causal masking is not supported yet (CTX_ERR_UNSUPPORTED).
+ */
+#ifndef CTX_ATTN_H
+#define CTX_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* ctx_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+/* Storage order of dense tensors: [B,S,H,D] or sequence-first [S,B,H,D]
+ * (the DeepSpeed layout of issue #7842, "Testcase"). */
+typedef enum { CTX_LAYOUT_BSHD = 0, CTX_LAYOUT_SBHD = 1 } ctx_layout_t;
+
+typedef enum {
+    CTX_OK = 0,
+    CTX_ERR_INVALID_ARG = 1, /* a size, pointer, stride or offset is invalid */
+    CTX_ERR_UNSUPPORTED = 2, /* valid but not implemented (D, causal, alignment) */
+    CTX_ERR_WORKSPACE = 3,   /* workspace missing, too small or misaligned */
+    CTX_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
+    CTX_ERR_TIMEOUT = 5      /* a device-side wait ran out of time (see ctx_get_device_status) */
+} ctx_status_t;
+
+/* A logical [B,S,H,D] tensor.  data is a device pointer to element
+ * (0,0,0,0).  Strides are in elements, D stride is 1.  If stride_b,
+ * stride_s and stride_h are all 0 the tensor is dense in the call's layout
+ * and the library derives them.  Pointers and the B/S/H strides must be
+ * 16-byte aligned (multiples of 8 elements) for the TMA engine. */
+typedef struct {
+    void* data;
+    int64_t B, S, H, D;
+    int64_t stride_b, stride_s, stride_h;
+} ctx_tensor_t;
+
+/* Flags for ctx_attn_fwd. */
+#define CTX_FLAG_NONE 0
+/* Write each ring iteration's partial (O_i, LSE_i) to the workspace and merge
+ * them with a separate LSE-merge kernel, instead of merging online inside
+ * the attention kernel.  Same result up to fp32 rounding order. */
+#define CTX_FLAG_MATERIALIZE_PARTIALS 1
+
+/* Bytes of device workspace the calls need for these sizes and flags:
+ * max(forward, backward).  Returns 0 on invalid sizes. */
+size_t ctx_attn_workspace_size(int B, int S, int Hq, int Hkv, int D, int P, int flags);
+
+/* Chunk table (host only, no GPU needed): writes P+1 offsets of the
+ * array_split chunking of S rows into P chunks.  CTX_ERR_INVALID_ARG if
+ * P < 1 or P > S. */
+int ctx_chunk_offsets(int S, int P, int* offsets_out);
+
+/* Ring-chunked attention forward.
+ *   q [B,S,Hq,D], k, v [B,S,Hkv,D] (bf16, read only);
+ *   out [B,S,Hq,D] (bf16, written), lse [B,Hq,S] fp32 contiguous (written):
+ *   lse = natural-log log-sum-exp of the scaled scores over all S keys.
+ * P ring chunks (1 <= P <= min(S, 64)).  workspace may be NULL unless
+ * CTX_FLAG_MATERIALIZE_PARTIALS is set.  Output rows are written once;
+ * out must not alias q, k or v. */
+int ctx_attn_fwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_t* v, int P,
+                 const int* chunk_offsets, ctx_layout_t layout, int causal, float scale,
+                 const ctx_tensor_t* out, float* lse, void* workspace, size_t workspace_bytes,
+                 int flags, ctx_stream_t stream);
+
+/* Ring-chunked attention backward.
+ *   q, k, v as in the forward; out, lse the forward's results; dout [B,S,Hq,D];
+ *   dq [B,S,Hq,D], dk, dv [B,S,Hkv,D] (bf16, written; for GQA dk, dv are
+ *   summed over the query heads of each kv head).
+ * workspace: at least ctx_attn_workspace_size(...) bytes, 256-byte aligned;
+ * it holds the fp32 dq accumulator and the per-row statistics. */
+int ctx_attn_bwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_t* v,
+                 const ctx_tensor_t* out, const float* lse, const ctx_tensor_t* dout, int P,
+                 const int* chunk_offsets, ctx_layout_t layout, int causal, float scale,
+                 const ctx_tensor_t* dq, const ctx_tensor_t* dk, const ctx_tensor_t* dv,
+                 void* workspace, size_t workspace_bytes, ctx_stream_t stream);
+
+/* Padded sequence length of the exchange: W * ceil(S / W), W = ring * ulysses. */
+int64_t ctx_exchange_padded_len(int64_t S, int ring, int ulysses);
+
+/* Ulysses sequence<->head exchange of 16-bit elements, bit-exact.
+ * W = ring * ulysses emulated ranks; rank rho = r * ulysses + u holds rows
+ * [rho * Ssh, (rho + 1) * Ssh) of the sequence padded with zero rows to
+ * Sp = W * Ssh, Ssh = ceil(S / W) (padding to a multiple of the world size:
+ * diffusers PR #12443 "Fix Flux Context Parallel Bug ...").  After the
+ * exchange rank (r, u) holds its ring group's ulysses shards in slot order
+ * and the head group [u*H/U, (u+1)*H/U) -- slot u' of a rank's output is the
+ * slot that rank owns in rank (r, u')'s input (DeepSpeed PR #8491, "Testing").
+ *
+ * x: the whole-sequence tensor [B,S,H,D] (strided like ctx_tensor_t).
+ * y: dense device buffer holding every rank's result, in the order
+ *    [U][B][Sp][H/U][D] for CTX_LAYOUT_BSHD, [U][Sp][B][H/U][D] for
+ *    CTX_LAYOUT_SBHD; rank (r, u) owns rows [r*U*Ssh, (r+1)*U*Ssh) of head
+ *    group u.  Pad rows are written as zero.
+ * dir 0: x -> y (sequence shards to head groups); dir 1: y -> x (the
+ * inverse, which is also the exchange's backward).  H % ulysses == 0. */
+int ctx_seq_head_exchange(const ctx_tensor_t* x, void* y, int ring, int ulysses, int dir,
+                          ctx_layout_t layout, ctx_stream_t stream);
+
+/* Synchronises the stream, then returns and clears the device status word
+ * that kernels set when a bounded wait ran out (CTX_ERR_TIMEOUT) or CTX_OK;
+ * CTX_ERR_CUDA if the synchronisation itself failed. */
+int ctx_get_device_status(ctx_stream_t stream);
+
+/* Failure-detection self test: launches one CTA whose single thread waits on
+ * an mbarrier that nothing ever arrives on, with a limit of timeout_us
+ * microseconds; the wait gives up, records CTX_ERR_TIMEOUT in the device
+ * status word and returns.  Nothing faults or hangs. */
+int ctx_selftest_wait_timeout(unsigned timeout_us, ctx_stream_t stream);
+
+/* Kernel timing for measurement.  While enabled, every launch of the
+ * attention forward kernel (kernel 0) and backward kernel (kernel 1) is
+ * bracketed by a pair of CUDA events recorded on the launch stream (at most
+ * 4096 launches per kernel are kept).  ctx_profile_enable(1) clears the
+ * records, ctx_profile_enable(0) stops recording.  ctx_profile_read waits for
+ * the recorded events and returns the summed device time of the kernel's
+ * launches in milliseconds and their number.  Host-side bookkeeping only;
+ * the events are created on first use. */
+int ctx_profile_enable(int enable);
+int ctx_profile_read(int kernel, double* total_ms, int* launches);
+
+/* Human-readable text of a status code. */
+const char* ctx_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CTX_ATTN_H */

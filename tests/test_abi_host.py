@@ -1,0 +1,156 @@
+"""Host-side checks of the C ABI library (no GPU needed): it builds for
+sm_103a, loads, exports every function include/ctx_attn.h declares, and its
+host-only logic (chunk table, workspace sizing, argument validation that
+happens before any launch) behaves as documented."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import context_attention_fwd_gb300 as ctx
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ctx_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return ctx.load_library(build_if_missing=True)
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(ctx_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert {"ctx_attn_fwd", "ctx_attn_bwd", "ctx_seq_head_exchange"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in ctx_attn.h but not exported"
+
+
+def test_library_is_built_for_sm103a():
+    so = ctx.library_path()
+    assert os.path.exists(so)
+    # the fatbinary names the architecture it carries; no other SASS is embedded
+    data = open(so, "rb").read()
+    assert b"sm_103a" in data
+
+
+@pytest.mark.parametrize("S,P", [(1001, 4), (32760, 8), (512, 2), (4608, 4), (5, 5), (17, 3), (65536, 4)])
+def test_chunk_table_matches_array_split(S, P):
+    assert ctx.chunk_offsets(S, P) == oracle.chunk_offsets(S, P)
+
+
+def test_chunk_table_examples():
+    off = ctx.chunk_offsets(1001, 4)
+    assert [b - a for a, b in zip(off[:-1], off[1:])] == [251, 250, 250, 250]
+    off = ctx.chunk_offsets(32760, 8)
+    assert all(b - a == 4095 for a, b in zip(off[:-1], off[1:]))
+
+
+def test_chunk_table_rejects_empty_chunks(lib):
+    arr = (ctypes.c_int * 8)()
+    assert lib.ctx_chunk_offsets(3, 4, arr) == 1
+    assert lib.ctx_chunk_offsets(3, 0, arr) == 1
+
+
+def test_workspace_size(lib):
+    # backward: two fp32 row-statistics arrays + the fp32 dq accumulator over
+    # 128-row tiles (each chunk padded to whole tiles)
+    n = lib.ctx_attn_workspace_size(1, 32760, 24, 24, 128, 8, 0)
+    slots = 24 * (8 * 32) * 128
+    assert n >= slots * 4 * 2 + slots * 128 * 4
+    assert lib.ctx_attn_workspace_size(1, 10, 6, 4, 64, 2, 0) == 0  # Hq % Hkv != 0
+    assert lib.ctx_attn_workspace_size(1, 10, 4, 4, 64, 11, 0) == 0  # P > S
+    # materialised partials need P * rows * (D + 1) fp32
+    n2 = lib.ctx_attn_workspace_size(1, 1000, 4, 4, 64, 4, 1)
+    assert n2 >= 4 * 4 * 1000 * 65 * 4
+
+
+def test_exchange_padded_len(lib):
+    assert lib.ctx_exchange_padded_len(65536, 4, 2) == 65536
+    assert lib.ctx_exchange_padded_len(1001, 4, 2) == 1008
+    assert lib.ctx_exchange_padded_len(10, 1, 2) == 10
+    assert lib.ctx_exchange_padded_len(0, 1, 2) == -1
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert lib.ctx_status_string(code)
+    assert b"timed out" in lib.ctx_status_string(5)
+
+
+def _t(data, B, S, H, D):
+    return ctx._Tensor(data, B, S, H, D, 0, 0, 0)
+
+
+def test_invalid_arguments_fail_before_launch(lib):
+    """Validation runs on the host and writes nothing; these calls need no GPU."""
+    fake = 1 << 20  # never dereferenced: validation fails first
+    lse = ctypes.c_void_p(fake)
+    q = _t(fake, 1, 64, 4, 64)
+    kv = _t(fake, 1, 64, 2, 64)
+    out = _t(fake, 1, 64, 4, 64)
+    call = lambda **kw: lib.ctx_attn_fwd(
+        ctypes.byref(kw.get("q", q)), ctypes.byref(kw.get("k", kv)), ctypes.byref(kw.get("v", kv)),
+        kw.get("P", 2), None, kw.get("layout", 0), kw.get("causal", 0), 0.0,
+        ctypes.byref(kw.get("out", out)), kw.get("lse", lse), None, 0, kw.get("flags", 0), None)
+    assert call(P=0) == 1                               # P < 1
+    assert call(P=65) == 1                              # P > S
+    assert call(k=_t(fake, 1, 64, 3, 64), v=_t(fake, 1, 64, 3, 64)) == 1  # Hq % Hkv
+    assert call(layout=7) == 1
+    assert call(lse=None) == 1
+    assert call(q=_t(fake, 1, 64, 4, 96), k=_t(fake, 1, 64, 2, 96), v=_t(fake, 1, 64, 2, 96),
+                out=_t(fake, 1, 64, 4, 96)) == 2        # D = 96 unsupported
+    assert call(causal=1) == 2                          # causal not implemented yet
+    assert call(out=_t(fake, 1, 63, 4, 64)) == 1        # shape mismatch
+    assert call(q=_t(fake + 2, 1, 64, 4, 64)) == 2      # misaligned for TMA
+    assert call(flags=1) == 3                           # partials need a workspace
+    assert call(flags=4) == 1                           # unknown flag
+    offs = (ctypes.c_int * 3)(0, 40, 63)                # must end at S
+    assert lib.ctx_attn_fwd(ctypes.byref(q), ctypes.byref(kv), ctypes.byref(kv), 2, offs, 0, 0, 0.0,
+                            ctypes.byref(out), lse, None, 0, 0, None) == 1
+    offs = (ctypes.c_int * 3)(0, 0, 64)                 # empty chunk
+    assert lib.ctx_attn_fwd(ctypes.byref(q), ctypes.byref(kv), ctypes.byref(kv), 2, offs, 0, 0, 0.0,
+                            ctypes.byref(out), lse, None, 0, 0, None) == 1
+
+
+def test_bwd_invalid_arguments(lib):
+    fake = 1 << 20
+    q = _t(fake, 1, 64, 4, 64)
+    kv = _t(fake, 1, 64, 2, 64)
+    lse = ctypes.c_void_p(fake)
+    args = [ctypes.byref(q), ctypes.byref(kv), ctypes.byref(kv), ctypes.byref(q), lse,
+            ctypes.byref(q), 2, None, 0, 0, 0.0, ctypes.byref(q), ctypes.byref(kv), ctypes.byref(kv)]
+    assert lib.ctx_attn_bwd(*args, None, 0, None) == 3                 # no workspace
+    assert lib.ctx_attn_bwd(*args, ctypes.c_void_p(fake), 16, None) == 3  # too small
+    need = lib.ctx_attn_workspace_size(1, 64, 4, 2, 64, 2, 0)
+    assert lib.ctx_attn_bwd(*args, ctypes.c_void_p(fake + 16), need, None) == 3  # misaligned
+    bad = list(args)
+    bad[6] = 0
+    assert lib.ctx_attn_bwd(*bad, ctypes.c_void_p(fake), need, None) == 1
+
+
+def test_exchange_invalid_arguments(lib):
+    fake = 1 << 20
+    x = _t(fake, 1, 16, 6, 64)
+    assert lib.ctx_seq_head_exchange(ctypes.byref(x), ctypes.c_void_p(fake), 2, 4, 0, 0, None) == 1  # H % U
+    assert lib.ctx_seq_head_exchange(ctypes.byref(x), ctypes.c_void_p(fake), 2, 2, 3, 0, None) == 1  # dir
+    assert lib.ctx_seq_head_exchange(ctypes.byref(x), None, 2, 2, 0, 0, None) == 1
+    assert lib.ctx_seq_head_exchange(ctypes.byref(x), ctypes.c_void_p(fake + 8), 2, 2, 0, 0, None) == 2
+
+
+def test_product_path_does_not_import_the_oracle():
+    """The library package never routes through oracle/ (no CPU fallback)."""
+    pkg = os.path.join(ROOT, "context_attention_fwd_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.lower(), f

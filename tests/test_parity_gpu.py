@@ -1,0 +1,186 @@
+"""GPU parity of the ring-chunked attention forward and backward against the
+fp64 oracle, through the C ABI.
+
+Tolerance (bf16 inputs, fp32 accumulation, bf16 outputs): per tensor both
+  ||got - ref||_2 / ||ref||_2 <= 2e-2   and   max|got - ref| / max|ref| <= 2e-2.
+lse (fp32 output) is held to 1e-3 absolute.
+"""
+import math
+
+import pytest
+import torch
+
+import context_attention_fwd_gb300 as ctx
+import oracle
+from seeded_inputs import (FLUX_GQA_S4608_P4, MHA_B2_S512_P2, SEQFIRST_S1001_P4, VIDEO_S32760_P8,
+                           AttnShape, attn_inputs)
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-2
+LSE_TOL = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ctx.load_library(build_if_missing=True)
+    yield
+    assert ctx.device_status() == 0
+
+
+def check(name, got, ref, tol=TOL):
+    g, r = got.double().cpu(), ref.double().cpu()
+    assert torch.isfinite(g).all(), f"{name}: non-finite values"
+    nrm = ((g - r).norm() / r.norm()).item()
+    mx = ((g - r).abs().max() / r.abs().max()).item()
+    assert nrm <= tol and mx <= tol, f"{name}: norm-rel {nrm:.3e}, max-rel {mx:.3e}"
+    return nrm, mx
+
+
+def run_gpu(shape, P=None, offsets=None, flags=0):
+    q, k, v, do = attn_inputs(shape)
+    qd, kd, vd, dod = (t.to("cuda") for t in (q, k, v, do))  # .to() keeps the storage order
+    if shape.layout == "sbhd" and shape.B > 1:
+        assert qd.stride(1) > qd.stride(0)
+    P = shape.P if P is None else P
+    out, lse = ctx.attn_fwd(qd, kd, vd, P, chunk_offsets=offsets, flags=flags)
+    dq, dk, dv = ctx.attn_bwd(qd, kd, vd, out, lse, dod, P, chunk_offsets=offsets)
+    torch.cuda.synchronize()
+    assert ctx.device_status() == 0
+    return (q, k, v, do), (out, lse, dq, dk, dv)
+
+
+def check_full(inputs, outputs):
+    q, k, v, do = inputs
+    out, lse, dq, dk, dv = outputs
+    o_ref, l_ref = oracle.attn_fwd(q, k, v)
+    check("out", out, o_ref)
+    assert (lse.double().cpu() - l_ref).abs().max() < LSE_TOL
+    dq_r, dk_r, dv_r = oracle.attn_bwd(q, k, v, do)
+    check("dq", dq, dq_r)
+    check("dk", dk, dk_r)
+    check("dv", dv, dv_r)
+
+
+def test_mha_b2_s512_p2():
+    check_full(*run_gpu(MHA_B2_S512_P2))
+
+
+def test_seqfirst_s1001_p4_uneven():
+    """Sequence-first storage, chunks 251/250/250/250 (not tile multiples)."""
+    inputs, outputs = run_gpu(SEQFIRST_S1001_P4)
+    assert outputs[0].stride(1) == 16 * 64  # output kept sequence-first
+    check_full(inputs, outputs)
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("D", [64, 128])
+def test_every_p_gqa(P, D):
+    sh = AttnShape(B=1, S=777, Hq=4, Hkv=2, D=D, P=P)
+    check_full(*run_gpu(sh))
+
+
+def test_custom_chunk_offsets():
+    sh = AttnShape(B=2, S=700, Hq=2, Hkv=1, D=128, P=4)
+    check_full(*run_gpu(sh, offsets=[0, 1, 300, 429, 700]))
+
+
+@pytest.mark.parametrize("S,P", [(1, 1), (5, 5), (130, 1), (257, 2), (128, 1), (129, 3)])
+def test_edge_sizes(S, P):
+    """Single rows, one-row chunks (P == S), tile tails of 1 and 2 rows."""
+    sh = AttnShape(B=1, S=S, Hq=2, Hkv=2, D=64, P=P)
+    inputs, outputs = run_gpu(sh)
+    if S == 1:
+        # closed form: one key, out = v, dq = dk = 0, dv = dout
+        q, k, v, do = inputs
+        out, lse, dq, dk, dv = outputs
+        assert torch.equal(out.cpu(), v.expand_as(out))
+        # dP - delta is zero up to fp32 summation order
+        assert dq.abs().max().item() < 1e-3 and dk.abs().max().item() < 1e-3
+        assert torch.equal(dv.cpu(), do)
+    else:
+        check_full(inputs, outputs)
+
+
+def test_materialized_partials_match_online():
+    """Per-iteration partials + the LSE-merge kernel give the oracle's result."""
+    sh = AttnShape(B=1, S=1001, Hq=4, Hkv=4, D=64, P=4, layout="sbhd")
+    inputs, outputs = run_gpu(sh, flags=ctx.FLAG_MATERIALIZE_PARTIALS)
+    check_full(inputs, outputs)
+    sh2 = AttnShape(B=2, S=600, Hq=4, Hkv=2, D=128, P=5)
+    check_full(*run_gpu(sh2, flags=ctx.FLAG_MATERIALIZE_PARTIALS))
+
+
+def test_results_independent_of_p():
+    """Every P computes the same attention: compare P=1 with P=8 on the GPU."""
+    sh = AttnShape(B=1, S=2048, Hq=4, Hkv=4, D=128, P=1)
+    _, o1 = run_gpu(sh, P=1)
+    inputs, o8 = run_gpu(sh, P=8)
+    for name, a, b in zip(("out", "lse", "dq", "dk", "dv"), o1, o8):
+        if name == "lse":
+            assert (a - b).abs().max().item() < LSE_TOL
+        else:
+            check(name, a, b, tol=1e-2)
+
+
+def test_flux_gqa_s4608_p4_sampled():
+    """Flux-like joint sequence, GQA 24/8, D=128: full forward of three heads
+    and sampled backward rows against the oracle."""
+    inputs, outputs = run_gpu(FLUX_GQA_S4608_P4)
+    q, k, v, do = inputs
+    out, lse, dq, dk, dv = outputs
+    sh = FLUX_GQA_S4608_P4
+    g = torch.Generator().manual_seed(1)
+    rows = [(0, int(h), int(s)) for h, s in zip(torch.randint(0, sh.Hq, (48,), generator=g),
+                                                torch.randint(0, sh.S, (48,), generator=g))]
+    rows += [(0, 5, s) for s in (0, 1151, 1152, 2303, 2304, 3455, 3456, 4607)]  # chunk edges
+    o_ref, l_ref = oracle.fwd_rows(q, k, v, rows)
+    got = torch.stack([out[b, s, h].cpu() for b, h, s in rows])
+    check("out rows", got, o_ref)
+    assert max(abs(lse[b, h, s].item() - l_ref[i].item()) for i, (b, h, s) in enumerate(rows)) < LSE_TOL
+    dq_ref = oracle.dq_rows(q, k, v, do, rows)
+    check("dq rows", torch.stack([dq[b, s, h].cpu() for b, h, s in rows]), dq_ref)
+    krows = [(0, hk, s) for hk in (0, 7) for s in (0, 5, 1151, 1152, 2000, 3456, 4607)]
+    dk_ref, dv_ref = oracle.dkv_rows(q, k, v, do, krows)
+    check("dk rows", torch.stack([dk[b, s, h].cpu() for b, h, s in krows]), dk_ref)
+    check("dv rows", torch.stack([dv[b, s, h].cpu() for b, h, s in krows]), dv_ref)
+
+
+def test_video_s32760_p8_full_size_sampled():
+    """The long-context workload at full size (in the launch configuration the
+    bench times): sampled rows at chunk and tile edges against the oracle,
+    plus properties that hold at any size."""
+    sh = VIDEO_S32760_P8
+    inputs, outputs = run_gpu(sh)
+    q, k, v, do = inputs
+    out, lse, dq, dk, dv = outputs
+    off = oracle.chunk_offsets(sh.S, sh.P)
+    edges = sorted({o + d for o in off for d in (-1, 0, 127, 128) if 0 <= o + d < sh.S})
+    rows = [(0, h, s) for h, s in zip([0, 7, 13, 23] * 16, edges[:64])]
+    o_ref, l_ref = oracle.fwd_rows(q, k, v, rows)
+    check("out rows", torch.stack([out[b, s, h].cpu() for b, h, s in rows]), o_ref)
+    assert max(abs(lse[b, h, s].item() - l_ref[i].item()) for i, (b, h, s) in enumerate(rows)) < LSE_TOL
+    qrows = rows[:24]
+    check("dq rows", torch.stack([dq[b, s, h].cpu() for b, h, s in qrows]),
+          oracle.dq_rows(q, k, v, do, qrows))
+    krows = [(0, 11, s) for s in edges[:16]]
+    dk_ref, dv_ref = oracle.dkv_rows(q, k, v, do, krows)
+    check("dk rows", torch.stack([dk[b, s, h].cpu() for b, h, s in krows]), dk_ref)
+    check("dv rows", torch.stack([dv[b, s, h].cpu() for b, h, s in krows]), dv_ref)
+    # at any size: sum_j dk_j = 0 and sum_j dv_j = sum_i do_i per head (fp32 sums)
+    dv_sum = dv.float().sum(dim=1)
+    do_sum = do.float().sum(dim=1).to(dv_sum.device)
+    assert ((dv_sum - do_sum).norm() / do_sum.norm()).item() < 2e-2
+    assert (dk.float().sum(dim=1).abs().max() / dk.float().abs().sum(dim=1).max()).item() < 2e-2
+
+
+def test_timeout_selftest_reports_status():
+    """A device wait that nothing satisfies gives up and reports CTX_ERR_TIMEOUT."""
+    assert ctx.device_status() == 0
+    ctx.selftest_wait_timeout(20000)
+    assert ctx.device_status() == 5
+    assert ctx.device_status() == 0  # reading clears it
+    # the context is still usable
+    sh = AttnShape(B=1, S=300, Hq=2, Hkv=2, D=64, P=2)
+    check_full(*run_gpu(sh))
