@@ -172,6 +172,29 @@ def config_dict():
             "P": sh.P, "layout": sh.layout, "causal": False, "l2": L2_NOTE}
 
 
+def measure_exchange(ctx, dev, stream, barrier, peaks):
+    """Ulysses exchange of the hybrid workload's q, [1,65536,32,128] bf16,
+    ring 4 x ulysses 2: forward and inverse, bytes read + written."""
+    xq = exchange_input(1, 65536, 32, 128, seed=5).to(dev)
+    y = ctx.seq_head_exchange(xq, 4, 2, 0, "bshd")
+    back = ctx.seq_head_exchange(y, 4, 2, 1, "bshd", S=65536, B=1, H=32)
+    barrier()
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 10
+    x0.record(stream)
+    for _ in range(reps):
+        ctx.seq_head_exchange(xq, 4, 2, 0, "bshd", y=y)
+        ctx.seq_head_exchange(y, 4, 2, 1, "bshd", y=back, S=65536, B=1, H=32)
+    x1.record(stream)
+    barrier()
+    xms = x0.elapsed_time(x1) / (2 * reps)
+    xbytes = 2 * xq.numel() * xq.element_size()
+    gbs = xbytes / (xms / 1e3) / 1e9
+    return {"shape": [1, 65536, 32, 128], "ring": 4, "ulysses": 2, "bound": "hbm", "achieved": gbs,
+            "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"], "ms": xms,
+            "bytes": xbytes}
+
+
 def source_sha(path):
     with open(path, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()
@@ -185,9 +208,18 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-exchange", action="store_true")
+    ap.add_argument("--shape", default=None,
+                    help="S,Hq,Hkv,D,P: a smaller case of the same kernels (profiler captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()
+    global WORKLOAD, WORKLOAD_NAME, L2_NOTE
+    if args.shape:
+        S, Hq, Hkv, D, P = (int(x) for x in args.shape.split(","))
+        WORKLOAD = AttnShape(B=1, S=S, Hq=Hq, Hkv=Hkv, D=D, P=P)
+        WORKLOAD_NAME = f"profiling case B=1 S={S} Hq={Hq} Hkv={Hkv} D={D} P={P}"
+        L2_NOTE = f"q/k/v/dout {4 * S * Hq * D * 2 / 1e6:.0f} MB; no flush"
 
     if args.impl == "reference":
         run_reference(args, world, rank)
@@ -295,22 +327,9 @@ def main():
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems / args.steps}
 
     # ------------------------------------------------ the exchange (HBM bound)
-    xq = exchange_input(1, 65536, 32, 128, seed=5).to(dev)
-    y = ctx.seq_head_exchange(xq, 4, 2, 0, "bshd")
-    back = ctx.seq_head_exchange(y, 4, 2, 1, "bshd", S=65536, B=1, H=32)
-    barrier()
-    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    reps = 10
-    x0.record(stream)
-    for _ in range(reps):
-        ctx.seq_head_exchange(xq, 4, 2, 0, "bshd", y=y)
-        ctx.seq_head_exchange(y, 4, 2, 1, "bshd", y=back, S=65536, B=1, H=32)
-    x1.record(stream)
-    barrier()
-    xms = x0.elapsed_time(x1) / (2 * reps)
-    xbytes = 2 * xq.numel() * xq.element_size()
-    x_gbs = xbytes / (xms / 1e3) / 1e9
-    del xq, y, back
+    exchange = None
+    if not args.no_exchange:
+        exchange = measure_exchange(ctx, dev, stream, barrier, peaks)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -321,7 +340,7 @@ def main():
                         "sustained": 100.0 * value / world / peaks["bf16_sustained"],
                         "peaks_source": peaks["source"]},
         "clocks": clocks,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 4 * args.steps + (0 if args.no_e2e else 4 * (args.steps + 2)),
         "roofline": {"kernel": "attn_bwd_kernel<128>", "bound": "tensor", "achieved": bwd_tf,
                      "peak": peak, "unit": "TFLOP/s", "frac": bwd_tf / peak, "traffic": traffic,
                      "peak_kind": f"bf16 dense, sustained ({peaks['source']})",
@@ -329,9 +348,7 @@ def main():
         "roofline_fwd": {"kernel": "attn_fwd_kernel<128>", "bound": "tensor", "achieved": fwd_tf,
                          "peak": peak, "unit": "TFLOP/s", "frac": fwd_tf / peak,
                          "launches": fwd_n, "avg_ms": fwd_avg},
-        "exchange": {"shape": [1, 65536, 32, 128], "ring": 4, "ulysses": 2, "bound": "hbm",
-                     "achieved": x_gbs, "peak": peaks["hbm"], "unit": "GB/s",
-                     "frac": x_gbs / peaks["hbm"], "ms": xms},
+        "exchange": exchange,
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
