@@ -7,6 +7,8 @@
 #include <stdio.h>
 #include <stdlib.h>
 
+#include <mutex>
+
 #include "../../include/ctx_attn.h"
 #include "internal.h"
 #include "ptx.cuh"
@@ -481,6 +483,50 @@ int ctx_attn_bwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
         if ((rc = launch_status())) return rc;
     }
     return CTX_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Scratch of ctx_attn_bwd_noalloc: a file-scope device array, so the entry
+// point needs no allocation.  Host code only sees a stand-in symbol; the
+// device address is looked up once per device with that device current.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[CTX_NOALLOC_SCRATCH_BYTES];
+
+void* noalloc_scratch_ptr() {
+    static std::mutex mu;
+    static void* ptrs[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        ptrs[dev] = p;
+    }
+    return ptrs[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+int ctx_attn_bwd_noalloc(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_t* v,
+                         const ctx_tensor_t* out, const float* lse, const ctx_tensor_t* dout, int P,
+                         const int* chunk_offsets, ctx_layout_t layout, int causal, float scale,
+                         const ctx_tensor_t* dq, const ctx_tensor_t* dk, const ctx_tensor_t* dv,
+                         ctx_stream_t stream) {
+    if (!q || !k) return CTX_ERR_INVALID_ARG;
+    if (q->B > INT32_MAX || q->S > INT32_MAX || q->H > INT32_MAX || k->H > INT32_MAX || q->D > INT32_MAX)
+        return CTX_ERR_INVALID_ARG;
+    const size_t need = ctx_attn_workspace_size((int)q->B, (int)q->S, (int)q->H, (int)k->H, (int)q->D, P, 0);
+    if (need == 0) return CTX_ERR_INVALID_ARG;
+    if (need > (size_t)CTX_NOALLOC_SCRATCH_BYTES) return CTX_ERR_WORKSPACE;
+    void* scratch = noalloc_scratch_ptr();
+    if (!scratch) return CTX_ERR_CUDA;
+    return ctx_attn_bwd(q, k, v, out, lse, dout, P, chunk_offsets, layout, causal, scale, dq, dk, dv,
+                        scratch, (size_t)CTX_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 int ctx_seq_head_exchange(const ctx_tensor_t* x, void* y, int ring, int ulysses, int dir,

@@ -111,6 +111,34 @@ int ctx_attn_bwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
                  const ctx_tensor_t* dq, const ctx_tensor_t* dk, const ctx_tensor_t* dv,
                  void* workspace, size_t workspace_bytes, ctx_stream_t stream);
 
+/* Backward without any device allocation by the caller.
+ *
+ * For callers that cannot call cudaMalloc: hosts whose device memory is
+ * owned by a framework allocator or reserved up front (a raw allocation
+ * would break the pool's accounting or fail under its budget), and code
+ * that must not trigger the implicit device-wide synchronisation of
+ * cudaFree.  Such callers still own q, k, v, out, lse, dout, dq, dk, dv; the
+ * scratch that ctx_attn_bwd takes as `workspace` comes instead from a
+ * file-scope device array of CTX_NOALLOC_SCRATCH_BYTES inside this library
+ * (every GPU that loads the library holds it until the process exits).
+ *
+ * Arguments and results are those of ctx_attn_bwd.  Problems whose scratch
+ * (ctx_attn_workspace_size with flags 0) exceeds CTX_NOALLOC_SCRATCH_BYTES
+ * are rejected with CTX_ERR_WORKSPACE before anything is launched.  The
+ * first call on a device looks up the array's device address on that device
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  The call allocates nothing and frees nothing.
+ * All calls share the one array and it keeps the last call's contents (the
+ * parts that must start at zero are cleared on every call): calls that
+ * overlap on the GPU, from different streams or threads, race on it.
+ * The pages have no counterpart of this entry point. */
+#define CTX_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+int ctx_attn_bwd_noalloc(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_t* v,
+                         const ctx_tensor_t* out, const float* lse, const ctx_tensor_t* dout, int P,
+                         const int* chunk_offsets, ctx_layout_t layout, int causal, float scale,
+                         const ctx_tensor_t* dq, const ctx_tensor_t* dk, const ctx_tensor_t* dv,
+                         ctx_stream_t stream);
+
 /* Padded sequence length of the exchange: W * ceil(S / W), W = ring * ulysses. */
 int64_t ctx_exchange_padded_len(int64_t S, int ring, int ulysses);
 
