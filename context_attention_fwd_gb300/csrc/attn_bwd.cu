@@ -22,11 +22,17 @@
 // dQ tiles are added into an fp32 accumulator in global memory (vector
 // reductions); dK, dV stay in TMEM for the whole CTA and are written once.
 //
-// Warp roles (320 threads):
-//   warp 0      TMA producer (K, V once; Q, dO, lse, delta per query tile, 2 stages)
-//   warp 1      TMEM owner and MMA issuer
-//   warps 2..5  P / dS math, one KV row per thread; dV epilogue
-//   warps 6..9  dQ drain (one query row per thread); dK epilogue
+// Warp roles (448 threads):
+//   warps 0..7   P / dS math: one KV row per thread (TMEM lane quarter =
+//                warp mod 4), warps 0..3 take query columns 0..63 and warps
+//                4..7 columns 64..127; dV epilogue (half the columns each)
+//   warps 8..11  dQ drain (one query row per thread); dK epilogue
+//   warp 12      TMA producer (K, V once; Q, dO, lse, delta per query tile, 2 stages)
+//   warp 13      TMEM owner and MMA issuer
+// P^T is written back into the S^T columns it was computed from (bf16
+// pairs): columns 0..31 for query columns 0..63, columns 96..127 for query
+// columns 64..127, so the two math warps of a lane quarter never overwrite
+// scores the other still has to read.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -61,7 +67,11 @@ struct BwdBars {
     int abort_flag;
 };
 
-constexpr int kMathThreads = 128;
+constexpr int kMathWarps = 8;
+constexpr int kMathThreads = 32 * kMathWarps;
+constexpr int kDrainThreads = 128;
+constexpr int kThreads = 448;
+constexpr int kProducerWarp = 12, kMmaWarp = 13;
 
 __device__ __forceinline__ int pick3(int o, int s, int h, int b) {
     return o == 0 ? s : (o == 1 ? h : b);
@@ -90,7 +100,7 @@ struct QTileIter {
 };
 
 template <int D>
-__global__ void __launch_bounds__(320, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
     using L = BwdLayout<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
     BwdBars& bars = *reinterpret_cast<BwdBars*>(smem + L::OFF_BARS);
@@ -118,7 +128,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_kernel(const __grid_constant_
         mbar_init(smem_u32(&bars.kv_full), 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&bars.q_full[i]), 1);
-            mbar_init(smem_u32(&bars.q_empty[i]), 1 + 4);  // MMA commit + one per math warp
+            mbar_init(smem_u32(&bars.q_empty[i]), 1 + kMathWarps);  // MMA commit + one per math warp
         }
         mbar_init(smem_u32(&bars.s_full), 1);
         mbar_init(smem_u32(&bars.dp_full), 1);
@@ -126,12 +136,12 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_kernel(const __grid_constant_
         mbar_init(smem_u32(&bars.ds_ready), kMathThreads);
         mbar_init(smem_u32(&bars.ds_free), 1);
         mbar_init(smem_u32(&bars.dq_full), 1);
-        mbar_init(smem_u32(&bars.dq_drained), kMathThreads);
+        mbar_init(smem_u32(&bars.dq_drained), kDrainThreads);
         mbar_init(smem_u32(&bars.final_mma), 1);
         mbar_init(smem_u32(&bars.drain), 1);
         mbar_fence_init();
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(&bars.tmem_slot), L::TM_COLS);
         tmem_relinquish();
     }
@@ -159,7 +169,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_kernel(const __grid_constant_
     q0.r = c;
     q0.t = ct.tile_off[c];
 
-    if (warp == 0) {
+    if (warp == kProducerWarp) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
             tma_prefetch_desc(&p.tq.map);
@@ -197,7 +207,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_kernel(const __grid_constant_
                     if (last_ph[st] >= 0) drain_wait(smem_u32(&bars.q_full[st]), last_ph[st], p.timeout_ns);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t id_st = idesc_bf16_f32(128, 128, false, false);  // K-major A and B
@@ -233,7 +243,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_kernel(const __grid_constant_
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)
-                    mma_ts(tmem + L::TM_DV, tmem + L::TM_S + kk * 8,
+                    mma_ts(tmem + L::TM_DV, tmem + L::TM_S + (kk < 4 ? kk * 8 : 96 + (kk - 4) * 8),
                            sdesc_sw128(sDOs + kk * 2048, L::BOX, 1024), id_dv,
                            (i > 0 || kk > 0) ? 1u : 0u);
                 // dK += dS^T Q ; dQ = dS K
@@ -258,47 +268,46 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_kernel(const __grid_constant_
             mma_commit(smem_u32(&bars.drain));
             drain_wait(smem_u32(&bars.drain), 0, p.timeout_ns);
         }
-    } else if (warp < 6) {
+    } else if (warp < kMathWarps) {
         // ---------------------------------------------------------- P / dS math
         const int quarter = warp & 3;
-        const int row = quarter * 32 + lane;  // KV row of this thread
+        const int half = warp >> 2;            // query columns [64*half, 64*half + 64)
+        const int row = quarter * 32 + lane;   // KV row of this thread
         const uint32_t taddr = tmem + (uint32_t(quarter * 32) << 16);
+        const uint32_t s_cols = L::TM_S + half * 64, p_cols = L::TM_S + half * 96;
         const float sc = p.scale_log2;
         const bool row_valid = row < kv_len;
         bool ok = true;
         for (int i = 0; i < n_q; ++i) {
             const int st = i & 1, ph = (i >> 1) & 1;
-            const float* lse2 = stat_base + st * 256;
-            const float* delta = lse2 + 128;
+            const float4* lse2 = reinterpret_cast<const float4*>(stat_base + st * 256 + half * 64);
+            const float4* delta = reinterpret_cast<const float4*>(stat_base + st * 256 + 128 + half * 64);
             if (!(ok = mbar_wait(smem_u32(&bars.q_full[st]), ph, wc))) break;
             if (!(ok = mbar_wait(smem_u32(&bars.s_full), i & 1, wc))) break;
             tc_fence_after();
-            uint32_t pr[128];
-            tmem_ld32(taddr + L::TM_S + 0, pr);
-            tmem_ld32(taddr + L::TM_S + 32, pr + 32);
-            tmem_ld32(taddr + L::TM_S + 64, pr + 64);
-            tmem_ld32(taddr + L::TM_S + 96, pr + 96);
+            uint32_t pr[64];
+            tmem_ld32(taddr + s_cols, pr);
+            tmem_ld32(taddr + s_cols + 32, pr + 32);
             tmem_ld_wait();
             reg_fence32(pr);
             reg_fence32(pr + 32);
-            reg_fence32(pr + 64);
-            reg_fence32(pr + 96);
             // P^T (fp32 kept in pr); padded query columns have lse2 = +inf -> 0
 #pragma unroll
-            for (int k = 0; k < 128; ++k) {
-                const float pv = ex2(fmaf(__uint_as_float(pr[k]), sc, -lse2[k]));
-                pr[k] = __float_as_uint(row_valid ? pv : 0.f);
+            for (int k4 = 0; k4 < 16; ++k4) {
+                const float4 l4 = lse2[k4];
+                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float pv = ex2(fmaf(__uint_as_float(pr[4 * k4 + e]), sc, -lv[e]));
+                    pr[4 * k4 + e] = __float_as_uint(row_valid ? pv : 0.f);
+                }
             }
             {
                 uint32_t pk[32];
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-#pragma unroll
-                    for (int k = 0; k < 32; ++k)
-                        pk[k] = pack_bf16x2(__uint_as_float(pr[64 * half + 2 * k]),
-                                            __uint_as_float(pr[64 * half + 2 * k + 1]));
-                    tmem_st32(taddr + L::TM_S + 32 * half, pk);
-                }
+                for (int k = 0; k < 32; ++k)
+                    pk[k] = pack_bf16x2(__uint_as_float(pr[2 * k]), __uint_as_float(pr[2 * k + 1]));
+                tmem_st32(taddr + p_cols, pk);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -307,26 +316,29 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_kernel(const __grid_constant_
             if (!(ok = mbar_wait(smem_u32(&bars.dp_full), i & 1, wc))) break;
             if (i > 0 && !(ok = mbar_wait(smem_u32(&bars.ds_free), (i - 1) & 1, wc))) break;
             tc_fence_after();
+            const uint32_t box = sDS + half * L::BOX;  // this half's 64 query columns
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
+            for (int cc = 0; cc < 2; ++cc) {
                 uint32_t dp[32];
-                tmem_ld32(taddr + L::TM_DP + cc * 32, dp);
+                tmem_ld32(taddr + L::TM_DP + half * 64 + cc * 32, dp);
                 tmem_ld_wait();
                 reg_fence32(dp);
                 uint32_t w[16];
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int q0i = cc * 32 + 2 * k;
-                    const float d0 = __uint_as_float(pr[q0i]) * (__uint_as_float(dp[2 * k]) - delta[q0i]);
-                    const float d1 =
-                        __uint_as_float(pr[q0i + 1]) * (__uint_as_float(dp[2 * k + 1]) - delta[q0i + 1]);
-                    w[k] = pack_bf16x2(d0, d1);
+                for (int k4 = 0; k4 < 8; ++k4) {
+                    const float4 d4 = delta[cc * 8 + k4];
+                    const int q0 = cc * 32 + 4 * k4;
+                    const float a0 = __uint_as_float(pr[q0 + 0]) * (__uint_as_float(dp[4 * k4 + 0]) - d4.x);
+                    const float a1 = __uint_as_float(pr[q0 + 1]) * (__uint_as_float(dp[4 * k4 + 1]) - d4.y);
+                    const float a2 = __uint_as_float(pr[q0 + 2]) * (__uint_as_float(dp[4 * k4 + 2]) - d4.z);
+                    const float a3 = __uint_as_float(pr[q0 + 3]) * (__uint_as_float(dp[4 * k4 + 3]) - d4.w);
+                    w[2 * k4] = pack_bf16x2(a0, a1);
+                    w[2 * k4 + 1] = pack_bf16x2(a2, a3);
                 }
                 // 32 query columns = four 16-byte chunks of the 128-byte swizzled row
-                const uint32_t box = sDS + (cc >> 1) * L::BOX;
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
-                    const uint32_t addr = box + sw128_offset(row, (cc & 1) * 4 + m);
+                    const uint32_t addr = box + sw128_offset(row, cc * 4 + m);
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[4 * m]),
                                  "r"(w[4 * m + 1]), "r"(w[4 * m + 2]), "r"(w[4 * m + 3])
                                  : "memory");
@@ -341,12 +353,13 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_kernel(const __grid_constant_
         // ---------------------------------------------------------- dV epilogue
         if (ok && mbar_wait(smem_u32(&bars.final_mma), 0, wc)) {
             tc_fence_after();
-            __nv_bfloat16* dst =
-                p.dv + (int64_t)b * p.k_sb + (int64_t)(kv_start + row) * p.k_ss + (int64_t)hk * p.k_sh;
+            constexpr int kHalfCols = D / 2;
+            __nv_bfloat16* dst = p.dv + (int64_t)b * p.k_sb + (int64_t)(kv_start + row) * p.k_ss +
+                                 (int64_t)hk * p.k_sh + half * kHalfCols;
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
+            for (int cc = 0; cc < kHalfCols / 32; ++cc) {
                 uint32_t o[32];
-                tmem_ld32(taddr + L::TM_DV + cc * 32, o);
+                tmem_ld32(taddr + L::TM_DV + half * kHalfCols + cc * 32, o);
                 tmem_ld_wait();
                 reg_fence32(o);
                 if (row_valid) {
@@ -361,7 +374,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_kernel(const __grid_constant_
                 }
             }
         }
-    } else {
+    } else if (warp < kMathWarps + 4) {
         // ---------------------------------------------------------- dQ drain
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;  // query row of the current tile
@@ -371,21 +384,27 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_kernel(const __grid_constant_
         for (int i = 0; i < n_q; ++i, next(q)) {
             if (!(ok = mbar_wait(smem_u32(&bars.dq_full), i & 1, wc))) break;
             tc_fence_after();
-            uint32_t v[D];
-#pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(taddr + L::TM_DP + cc * 32, v + cc * 32);
-            tmem_ld_wait();
-#pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) reg_fence32(v + cc * 32);
-            tc_fence_before();
-            mbar_arrive(smem_u32(&bars.dq_drained));
             // tile-major accumulator: [(b,h,t)][D/4][128 rows][4]
             float* tile = p.dq_acc + ((size_t)(b * p.Hq + q.h) * ct.ntiles + q.t) * (size_t)(kTile * D);
+            // 64 columns at a time; the TMEM columns are released after the last load
 #pragma unroll
-            for (int g = 0; g < D / 4; ++g)
-                red_add_v4(tile + ((size_t)g * kTile + row) * 4, __uint_as_float(v[4 * g]),
-                           __uint_as_float(v[4 * g + 1]), __uint_as_float(v[4 * g + 2]),
-                           __uint_as_float(v[4 * g + 3]));
+            for (int hc = 0; hc < D / 64; ++hc) {
+                uint32_t v[64];
+                tmem_ld32(taddr + L::TM_DP + hc * 64, v);
+                tmem_ld32(taddr + L::TM_DP + hc * 64 + 32, v + 32);
+                tmem_ld_wait();
+                reg_fence32(v);
+                reg_fence32(v + 32);
+                if (hc == D / 64 - 1) {
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(&bars.dq_drained));
+                }
+#pragma unroll
+                for (int g = 0; g < 16; ++g)
+                    red_add_v4(tile + ((size_t)(hc * 16 + g) * kTile + row) * 4, __uint_as_float(v[4 * g]),
+                               __uint_as_float(v[4 * g + 1]), __uint_as_float(v[4 * g + 2]),
+                               __uint_as_float(v[4 * g + 3]));
+            }
         }
         // ---------------------------------------------------------- dK epilogue
         if (ok && mbar_wait(smem_u32(&bars.final_mma), 0, wc)) {
@@ -417,7 +436,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_kernel(const __grid_constant_
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, L::TM_COLS);
+    if (warp == kMmaWarp) tmem_dealloc(tmem, L::TM_COLS);
 }
 
 template <int D>
@@ -427,7 +446,7 @@ int launch_bwd_d(const BwdParams& p, cudaStream_t s) {
                              L::SMEM) != cudaSuccess)
         return 4;
     dim3 grid(p.ct.ntiles, p.Hkv, p.B);
-    attn_bwd_kernel<D><<<grid, 320, L::SMEM, s>>>(p);
+    attn_bwd_kernel<D><<<grid, kThreads, L::SMEM, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
 
