@@ -214,20 +214,35 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             constexpr uint32_t id_dv = idesc_bf16_f32(128, D, false, true);     // A TMEM, B MN-major
             constexpr uint32_t id_dk = idesc_bf16_f32(128, D, false, true);     // A K-major smem, B MN-major
             constexpr uint32_t id_dq = idesc_bf16_f32(128, D, true, true);      // A MN-major, B MN-major
-            bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, wc);
-            for (int i = 0; i < n_q && ok; ++i) {
-                const int st = i & 1, ph = (i >> 1) & 1;
-                const uint32_t sQs = sQ + st * L::TILE, sDOs = sDO + st * L::TILE;
-                if (!(ok = mbar_wait(smem_u32(&bars.q_full[st]), ph, wc))) break;
-                tc_fence_after();
-                // S^T = K Q^T
+            // Tensor-core order per query tile i: dV_i, dP_i, S_{i+1}, dK_i, dQ_i.
+            // P_i is computed while dK_{i-1}, dQ_{i-1} run, dS_i while S_{i+1}
+            // runs, and dQ_{i-1} is drained from TMEM while dV_i runs.
+            auto issue_s = [&](int st) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t koff = (kk >> 2) * L::BOX + (kk & 3) * 32;
                     mma_ss(tmem + L::TM_S, sdesc_sw128(sK + koff, 16, 1024),
-                           sdesc_sw128(sQs + koff, 16, 1024), id_st, kk > 0 ? 1u : 0u);
+                           sdesc_sw128(sQ + st * L::TILE + koff, 16, 1024), id_st, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(smem_u32(&bars.s_full));
+            };
+            bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, wc) &&
+                      mbar_wait(smem_u32(&bars.q_full[0]), 0, wc);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);  // S^T_0 = K Q_0^T
+            }
+            for (int i = 0; i < n_q && ok; ++i) {
+                const int st = i & 1;
+                const uint32_t sQs = sQ + st * L::TILE, sDOs = sDO + st * L::TILE;
+                // dV += P^T dO
+                if (!(ok = mbar_wait(smem_u32(&bars.p_ready), i & 1, wc))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    mma_ts(tmem + L::TM_DV, tmem + L::TM_S + (kk < 4 ? kk * 8 : 96 + (kk - 4) * 8),
+                           sdesc_sw128(sDOs + kk * 2048, L::BOX, 1024), id_dv,
+                           (i > 0 || kk > 0) ? 1u : 0u);
                 // dP^T = V dO^T, into the columns the previous dQ occupied
                 if (i > 0 && !(ok = mbar_wait(smem_u32(&bars.dq_drained), (i - 1) & 1, wc))) break;
                 tc_fence_after();
@@ -238,14 +253,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                            sdesc_sw128(sDOs + koff, 16, 1024), id_st, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(smem_u32(&bars.dp_full));
-                // dV += P^T dO
-                if (!(ok = mbar_wait(smem_u32(&bars.p_ready), i & 1, wc))) break;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)
-                    mma_ts(tmem + L::TM_DV, tmem + L::TM_S + (kk < 4 ? kk * 8 : 96 + (kk - 4) * 8),
-                           sdesc_sw128(sDOs + kk * 2048, L::BOX, 1024), id_dv,
-                           (i > 0 || kk > 0) ? 1u : 0u);
+                // S^T of the next tile overwrites P^T_i, which dV above has read
+                // (tcgen05.mma from one thread execute in issue order)
+                if (i + 1 < n_q) {
+                    if (!(ok = mbar_wait(smem_u32(&bars.q_full[(i + 1) & 1]), ((i + 1) >> 1) & 1, wc))) break;
+                    tc_fence_after();
+                    issue_s((i + 1) & 1);
+                }
                 // dK += dS^T Q ; dQ = dS K
                 if (!(ok = mbar_wait(smem_u32(&bars.ds_ready), i & 1, wc))) break;
                 tc_fence_after();

@@ -1,11 +1,12 @@
 // attn_fwd.cu -- ring-chunked attention forward for sm_103a.
 //
-// One CTA owns one 128-row query tile of one (batch, query head).  The tile
-// belongs to ring chunk r; the CTA walks the ring iterations i = 0..P-1,
-// meeting KV chunk c = (r - i) mod P at iteration i (diffusers issue #14265,
-// "Root cause": the query stays put while the K/V chunks rotate), and within
-// an iteration the 128-row KV tiles of chunk c.  Keys past the chunk's end
-// are masked, so every iteration sees exactly its own chunk.
+// One CTA owns two 128-row query tiles (A and B, consecutive tiles of the
+// same ring chunk r) of one (batch, query head).  It walks the ring
+// iterations i = 0..P-1, meeting KV chunk c = (r - i) mod P at iteration i
+// (diffusers issue #14265, "Root cause": the query stays put while the K/V
+// chunks rotate), and within an iteration the 128-row KV tiles of chunk c.
+// Keys past the chunk's end are masked, so every iteration sees exactly its
+// own chunk.  Both query tiles share every K/V tile the CTA loads.
 //
 // Merging.  Each iteration's partial (O_i, LSE_i) is merged by LSE
 // weighting (same issue, "How it surfaces": the ring needs the LSE to merge
@@ -15,15 +16,16 @@
 // reset at every chunk boundary and (O_i / l_i, m_i + log l_i) is written out
 // for a separate merge kernel.
 //
-// Warp roles (192 threads):
-//   warp 0      TMA producer: Q once, K/V tiles through a 2-stage ring
-//   warp 1      TMEM owner and tcgen05.mma issuer (one elected lane)
-//   warps 2..5  softmax: one query row per thread, S from TMEM, P back to
-//               TMEM as bf16 (A operand of the PV product), O rescale,
-//               epilogue
-// TMEM (512 columns): S/P double buffer at columns 0 and 128, O at 256.
-// S = Q K^T: A = Q (smem, K-major), B = K (smem, K-major), M=N=128.
-// O += P V:  A = P (TMEM), B = V (smem, MN-major: V rows are the K index).
+// Warp roles (384 threads):
+//   warp 0       TMA producer: Q_A, Q_B once, K/V tiles through a 2-stage ring
+//   warp 1       TMEM owner and tcgen05.mma issuer (one elected lane)
+//   warps 2, 3   idle (keep the softmax warpgroups warpgroup-aligned)
+//   warps 4..7   softmax of tile A, warps 8..11 softmax of tile B: one query
+//                row per thread, S from TMEM, P back to TMEM as bf16 (A
+//                operand of the PV product), lazy O rescale, epilogue
+// TMEM (512 columns): S_A 0, S_B 128, O_A 256, O_B 256 + D.
+// Tensor-core order: S_A(j) S_B(j) PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) ...
+// so each softmax overlaps two products of the other tile.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -32,12 +34,12 @@ namespace {
 
 template <int D>
 struct FwdLayout {
-    static constexpr int NBOX = D / 64;                 // 128-byte swizzle boxes per row
-    static constexpr uint32_t BOX = kTile * 128;        // one box: 128 rows x 128 bytes
-    static constexpr uint32_t TILE = kTile * D * 2;     // a 128 x D bf16 tile
+    static constexpr int NBOX = D / 64;              // 128-byte swizzle boxes per row
+    static constexpr uint32_t BOX = kTile * 128;     // one box: 128 rows x 128 bytes
+    static constexpr uint32_t TILE = kTile * D * 2;  // a 128 x D bf16 tile
     static constexpr int STAGES = 2;
-    static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_K = OFF_Q + TILE;
+    static constexpr uint32_t OFF_Q = 0;              // Q_A, Q_B
+    static constexpr uint32_t OFF_K = OFF_Q + 2 * TILE;
     static constexpr uint32_t OFF_V = OFF_K + STAGES * TILE;
     static constexpr uint32_t END = OFF_V + STAGES * TILE;
     // Request enough shared memory that only one CTA fits per SM: each CTA
@@ -49,14 +51,15 @@ struct FwdLayout {
 struct FwdBars {
     uint64_t q_full;
     uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
-    uint64_t s_full[2], p_full[2];
-    uint64_t o_done;   // one arrival per PV product
-    uint64_t o_chunk;  // after the last PV of a chunk (every chunk with partials, else once)
-    uint64_t o_free;   // partials: O drained, the next chunk may overwrite it
-    uint64_t drain;    // teardown: all MMAs retired
+    uint64_t s_full[2], p_full[2];  // per query tile
+    uint64_t o_chunk[2];  // per tile: after the last PV of a chunk (every chunk with partials, else once)
+    uint64_t o_free[2];   // partials: O drained, the next chunk may overwrite it
+    uint64_t drain;       // teardown: all MMAs retired
 };
 
+constexpr int kThreads = 384;
 constexpr int kSoftmaxThreads = 128;
+constexpr int kSoftmaxWarp0 = 4;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: move the reference max lazily
 
 __device__ __forceinline__ int pick3(int o, int s, int h, int b) {
@@ -76,8 +79,30 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
         if (globaltimer_ns() - t0 > limit_ns) break;
 }
 
+// The KV tiles a query chunk r visits, in ring order: iteration it meets
+// chunk (r - it) mod P; tiles [t0, t1) belong to that chunk.
+struct KvWalk {
+    int it, c, t, t0, t1;
+};
+__device__ __forceinline__ void kv_first(const ChunkTable& ct, int r, KvWalk& w) {
+    w.it = 0;
+    w.c = r;
+    w.t0 = w.t = ct.tile_off[r];
+    w.t1 = ct.tile_off[r + 1];
+}
+__device__ __forceinline__ void kv_next(const ChunkTable& ct, int r, KvWalk& w) {
+    if (++w.t == w.t1) {
+        ++w.it;
+        if (w.it < ct.P) {
+            w.c = (r - w.it + ct.P) % ct.P;
+            w.t0 = w.t = ct.tile_off[w.c];
+            w.t1 = ct.tile_off[w.c + 1];
+        }
+    }
+}
+
 template <int D>
-__global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
     using L = FwdLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ FwdBars bars;
@@ -87,12 +112,15 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t sQ = sbase + L::OFF_Q, sK = sbase + L::OFF_K, sV = sbase + L::OFF_V;
     const int warp = warp_id(), lane = lane_id();
-    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int pair = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const ChunkTable& ct = p.ct;
     const int P = ct.P;
-    const int r = chunk_of_tile(ct, qt);
-    const int q_start = ct.off[r] + (qt - ct.tile_off[r]) * kTile;
-    const int q_len = min(kTile, ct.off[r + 1] - q_start);
+    int r = 0;
+    while (r + 1 < P && ct.pair_off[r + 1] <= pair) ++r;
+    const int tA = ct.tile_off[r] + 2 * (pair - ct.pair_off[r]);
+    const bool hasB = tA + 1 < ct.tile_off[r + 1];
+    const int ntile = hasB ? 2 : 1;
+    const int qs0 = ct.off[r] + (tA - ct.tile_off[r]) * kTile;
     const int hk = h / p.group;
     const int n_kv = ct.ntiles;
     const bool partials = p.part_o != nullptr;
@@ -108,10 +136,9 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
             mbar_init(smem_u32(&bars.v_empty[i]), 1);
             mbar_init(smem_u32(&bars.s_full[i]), 1);
             mbar_init(smem_u32(&bars.p_full[i]), kSoftmaxThreads);
+            mbar_init(smem_u32(&bars.o_chunk[i]), 1);
+            mbar_init(smem_u32(&bars.o_free[i]), kSoftmaxThreads);
         }
-        mbar_init(smem_u32(&bars.o_done), 1);
-        mbar_init(smem_u32(&bars.o_chunk), 1);
-        mbar_init(smem_u32(&bars.o_free), kSoftmaxThreads);
         mbar_init(smem_u32(&bars.drain), 1);
         mbar_fence_init();
     }
@@ -131,29 +158,29 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
             tma_prefetch_desc(&p.tk.map);
             tma_prefetch_desc(&p.tv.map);
             const uint32_t qf = smem_u32(&bars.q_full);
-            mbar_arrive_expect_tx(qf, L::TILE);
-            for (int bx = 0; bx < L::NBOX; ++bx)
-                tma_tile(p.tq, sQ + bx * L::BOX, qf, bx * 64, q_start, h, b);
-            int j = 0, last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
+            mbar_arrive_expect_tx(qf, ntile * L::TILE);
+            for (int x = 0; x < ntile; ++x)
+                for (int bx = 0; bx < L::NBOX; ++bx)
+                    tma_tile(p.tq, sQ + x * L::TILE + bx * L::BOX, qf, bx * 64, qs0 + x * kTile, h, b);
+            int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
             bool ok = true;
-            for (int it = 0; it < P && ok; ++it) {
-                const int c = (r - it + P) % P;
-                for (int t = ct.tile_off[c]; t < ct.tile_off[c + 1]; ++t, ++j) {
-                    const int st = j & 1, ph = (j >> 1) & 1;
-                    const int kv_start = ct.off[c] + (t - ct.tile_off[c]) * kTile;
-                    if (!(ok = mbar_wait(smem_u32(&bars.k_empty[st]), ph ^ 1, wc))) break;
-                    const uint32_t kf = smem_u32(&bars.k_full[st]);
-                    mbar_arrive_expect_tx(kf, L::TILE);
-                    for (int bx = 0; bx < L::NBOX; ++bx)
-                        tma_tile(p.tk, sK + st * L::TILE + bx * L::BOX, kf, bx * 64, kv_start, hk, b);
-                    last_k[st] = ph;
-                    if (!(ok = mbar_wait(smem_u32(&bars.v_empty[st]), ph ^ 1, wc))) break;
-                    const uint32_t vf = smem_u32(&bars.v_full[st]);
-                    mbar_arrive_expect_tx(vf, L::TILE);
-                    for (int bx = 0; bx < L::NBOX; ++bx)
-                        tma_tile(p.tv, sV + st * L::TILE + bx * L::BOX, vf, bx * 64, kv_start, hk, b);
-                    last_v[st] = ph;
-                }
+            KvWalk w;
+            kv_first(ct, r, w);
+            for (int j = 0; j < n_kv; ++j, kv_next(ct, r, w)) {
+                const int st = j & 1, ph = (j >> 1) & 1;
+                const int kv_start = ct.off[w.c] + (w.t - w.t0) * kTile;
+                if (!(ok = mbar_wait(smem_u32(&bars.k_empty[st]), ph ^ 1, wc))) break;
+                const uint32_t kf = smem_u32(&bars.k_full[st]);
+                mbar_arrive_expect_tx(kf, L::TILE);
+                for (int bx = 0; bx < L::NBOX; ++bx)
+                    tma_tile(p.tk, sK + st * L::TILE + bx * L::BOX, kf, bx * 64, kv_start, hk, b);
+                last_k[st] = ph;
+                if (!(ok = mbar_wait(smem_u32(&bars.v_empty[st]), ph ^ 1, wc))) break;
+                const uint32_t vf = smem_u32(&bars.v_full[st]);
+                mbar_arrive_expect_tx(vf, L::TILE);
+                for (int bx = 0; bx < L::NBOX; ++bx)
+                    tma_tile(p.tv, sV + st * L::TILE + bx * L::BOX, vf, bx * 64, kv_start, hk, b);
+                last_v[st] = ph;
             }
             if (!ok) {
                 // wait for our own copies in flight before the CTA retires
@@ -169,183 +196,194 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
-            bool ok = mbar_wait(smem_u32(&bars.q_full), 0, wc);
-            tc_fence_after();
-            // PV of the previous tile is issued after QK of the current one, so
-            // the tensor core computes S_{j+1} while the softmax works on S_j.
-            int j = 0, prev_it = 0;
-            bool prev_first = false, prev_last = false;
-            auto issue_pv = [&](int jp, bool first, bool last, int itp) -> bool {
-                const int stp = jp & 1, php = (jp >> 1) & 1;
-                if (!mbar_wait(smem_u32(&bars.p_full[stp]), php, wc)) return false;
-                if (!mbar_wait(smem_u32(&bars.v_full[stp]), php, wc)) return false;
-                if (partials && first && itp > 0 &&
-                    !mbar_wait(smem_u32(&bars.o_free), (itp - 1) & 1, wc))
+            // S_x = Q_x K^T for the K tile in stage st
+            auto issue_s = [&](int x, int st) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t koff = (kk >> 2) * L::BOX + (kk & 3) * 32;
+                    mma_ss(tmem + L::TM_S + x * 128, sdesc_sw128(sQ + x * L::TILE + koff, 16, 1024),
+                           sdesc_sw128(sK + st * L::TILE + koff, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(smem_u32(&bars.s_full[x]));
+            };
+            // O_x += P_x V for KV tile j (stage st); first/last: its position in its chunk
+            auto issue_pv = [&](int x, int j, int st, bool first, bool last, int it) -> bool {
+                if (!mbar_wait(smem_u32(&bars.p_full[x]), j & 1, wc)) return false;
+                if (partials && first && it > 0 && !mbar_wait(smem_u32(&bars.o_free[x]), (it - 1) & 1, wc))
                     return false;
                 tc_fence_after();
-                const bool acc0 = partials ? !first : jp > 0;
+                const bool acc0 = partials ? !first : j > 0;
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk) {
-                    const uint64_t bdesc = sdesc_sw128(sV + stp * L::TILE + kk * 2048, L::BOX, 1024);
-                    mma_ts(tmem + L::TM_O, tmem + L::TM_S + stp * 128 + kk * 8, bdesc, idesc_pv,
+                    const uint64_t bdesc = sdesc_sw128(sV + st * L::TILE + kk * 2048, L::BOX, 1024);
+                    mma_ts(tmem + L::TM_O + x * D, tmem + L::TM_S + x * 128 + kk * 8, bdesc, idesc_pv,
                            (acc0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(smem_u32(&bars.o_done));
-                mma_commit(smem_u32(&bars.v_empty[stp]));
-                if (last && (partials || itp == P - 1)) mma_commit(smem_u32(&bars.o_chunk));
+                if (last && (partials || it == P - 1)) mma_commit(smem_u32(&bars.o_chunk[x]));
                 return true;
             };
-            for (int it = 0; it < P && ok; ++it) {
-                const int c = (r - it + P) % P;
-                const int t0 = ct.tile_off[c], t1 = ct.tile_off[c + 1];
-                for (int t = t0; t < t1; ++t, ++j) {
-                    const int st = j & 1, ph = (j >> 1) & 1;
-                    if (!(ok = mbar_wait(smem_u32(&bars.k_full[st]), ph, wc))) break;
+            bool ok = mbar_wait(smem_u32(&bars.q_full), 0, wc) && mbar_wait(smem_u32(&bars.k_full[0]), 0, wc);
+            if (ok) {
+                tc_fence_after();
+                for (int x = 0; x < ntile; ++x) issue_s(x, 0);
+                mma_commit(smem_u32(&bars.k_empty[0]));
+            }
+            KvWalk w;
+            kv_first(ct, r, w);
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const int st = j & 1;
+                const bool first = w.t == w.t0, last = w.t == w.t1 - 1;
+                const int it = w.it;
+                kv_next(ct, r, w);
+                const bool more = j + 1 < n_kv;
+                const int st1 = (j + 1) & 1, ph1 = ((j + 1) >> 1) & 1;
+                if (!(ok = mbar_wait(smem_u32(&bars.v_full[st]), (j >> 1) & 1, wc))) break;
+                if (!(ok = issue_pv(0, j, st, first, last, it))) break;
+                if (more) {  // S_A(j+1) overwrites P_A(j): issued after PV_A(j), executed in order
+                    if (!(ok = mbar_wait(smem_u32(&bars.k_full[st1]), ph1, wc))) break;
                     tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t koff = (kk >> 2) * L::BOX + (kk & 3) * 32;
-                        mma_ss(tmem + L::TM_S + st * 128, sdesc_sw128(sQ + koff, 16, 1024),
-                               sdesc_sw128(sK + st * L::TILE + koff, 16, 1024), idesc_qk,
-                               kk > 0 ? 1u : 0u);
-                    }
-                    mma_commit(smem_u32(&bars.s_full[st]));
-                    mma_commit(smem_u32(&bars.k_empty[st]));
-                    if (j > 0 && !(ok = issue_pv(j - 1, prev_first, prev_last, prev_it))) break;
-                    prev_first = (t == t0);
-                    prev_last = (t == t1 - 1);
-                    prev_it = it;
+                    issue_s(0, st1);
+                }
+                if (hasB && !(ok = issue_pv(1, j, st, first, last, it))) break;
+                mma_commit(smem_u32(&bars.v_empty[st]));
+                if (more) {
+                    if (hasB) issue_s(1, st1);
+                    mma_commit(smem_u32(&bars.k_empty[st1]));
                 }
             }
-            if (ok && n_kv > 0) issue_pv(n_kv - 1, prev_first, prev_last, prev_it);
             mma_commit(smem_u32(&bars.drain));
             drain_wait(smem_u32(&bars.drain), 0, p.timeout_ns);
         }
-    } else {
+    } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4 * ntile) {
         // ------------------------------------------------------ softmax
+        const int x = (warp - kSoftmaxWarp0) >> 2;  // query tile A (0) or B (1)
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t taddr = tmem + (uint32_t(quarter * 32) << 16);
+        const uint32_t s_cols = L::TM_S + x * 128, o_cols = L::TM_O + x * D;
+        const int q_start = qs0 + x * kTile;
         const float sc = p.scale_log2;
+        const bool valid = row < ct.off[r + 1] - q_start;
         float m_ref = -INFINITY, l = 0.f;
-        int j = 0;
         bool ok = true;
-        for (int it = 0; it < P && ok; ++it) {
-            const int c = (r - it + P) % P;
-            const int t0 = ct.tile_off[c], t1 = ct.tile_off[c + 1];
-            for (int t = t0; t < t1; ++t, ++j) {
-                const int st = j & 1, ph = (j >> 1) & 1;
-                const int kv_len = min(kTile, ct.off[c + 1] - (ct.off[c] + (t - t0) * kTile));
-                const bool first = partials ? (t == t0) : (j == 0);
-                if (!(ok = mbar_wait(smem_u32(&bars.s_full[st]), ph, wc))) break;
+        KvWalk w;
+        kv_first(ct, r, w);
+        for (int j = 0; j < n_kv; ++j, kv_next(ct, r, w)) {
+            const int kv_len = min(kTile, ct.off[w.c + 1] - (ct.off[w.c] + (w.t - w.t0) * kTile));
+            const bool first = partials ? (w.t == w.t0) : (j == 0);
+            if (!(ok = mbar_wait(smem_u32(&bars.s_full[x]), j & 1, wc))) break;
+            tc_fence_after();
+            uint32_t s[128];
+            tmem_ld32(taddr + s_cols + 0, s);
+            tmem_ld32(taddr + s_cols + 32, s + 32);
+            tmem_ld32(taddr + s_cols + 64, s + 64);
+            tmem_ld32(taddr + s_cols + 96, s + 96);
+            tmem_ld_wait();
+            reg_fence32(s);
+            reg_fence32(s + 32);
+            reg_fence32(s + 64);
+            reg_fence32(s + 96);
+            if (kv_len < kTile) {
+#pragma unroll
+                for (int k = 0; k < 128; ++k)
+                    if (k >= kv_len) s[k] = __float_as_uint(-INFINITY);
+            }
+            float mx8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx8[e] = __uint_as_float(s[e]);
+#pragma unroll
+            for (int k = 8; k < 128; k += 8)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], __uint_as_float(s[k + e]));
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            if (first) {
+                m_ref = -INFINITY;
+                l = 0.f;
+            }
+            float alpha = 1.f;
+            bool rescale = false;
+            if (mx > m_ref) {
+                if (m_ref == -INFINITY) {
+                    m_ref = mx;  // nothing accumulated yet for this row
+                } else if ((mx - m_ref) * sc > kRescaleThreshold) {
+                    alpha = ex2((m_ref - mx) * sc);
+                    m_ref = mx;
+                    rescale = true;
+                }
+            }
+            const float neg = -m_ref * sc;
+            float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < 64; ++k) {
+                const float p0 = ex2(fmaf(__uint_as_float(s[2 * k]), sc, neg));
+                const float p1 = ex2(fmaf(__uint_as_float(s[2 * k + 1]), sc, neg));
+                sum8[(2 * k) & 7] += p0;
+                sum8[(2 * k + 1) & 7] += p1;
+                s[k] = pack_bf16x2(p0, p1);  // packed P overwrites scores already consumed
+            }
+            tmem_st32(taddr + s_cols + 0, s);
+            tmem_st32(taddr + s_cols + 32, s + 32);
+            const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                              ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+            l = l * alpha + sum;
+            if (__any_sync(0xffffffffu, rescale)) {
+                // PV of the previous KV tile was issued before this S and has
+                // completed with it: rescale O in place.
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t o[32];
+                    tmem_ld32(taddr + o_cols + cc * 32, o);
+                    tmem_ld_wait();
+                    reg_fence32(o);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                    tmem_st32(taddr + o_cols + cc * 32, o);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.p_full[x]));
+            if (partials && w.t == w.t1 - 1) {
+                // this chunk's partial is complete: O_it / l, LSE_it
+                const int it = w.it;
+                if (!(ok = mbar_wait(smem_u32(&bars.o_chunk[x]), it & 1, wc))) break;
                 tc_fence_after();
-                uint32_t s[128];
-                tmem_ld32(taddr + L::TM_S + st * 128 + 0, s);
-                tmem_ld32(taddr + L::TM_S + st * 128 + 32, s + 32);
-                tmem_ld32(taddr + L::TM_S + st * 128 + 64, s + 64);
-                tmem_ld32(taddr + L::TM_S + st * 128 + 96, s + 96);
-                tmem_ld_wait();
-                reg_fence32(s);
-                reg_fence32(s + 32);
-                reg_fence32(s + 64);
-                reg_fence32(s + 96);
-                if (kv_len < kTile) {
+                const float inv_l = 1.f / l;
+                const size_t prow = ((size_t)(it * p.B + b) * p.Hq + h) * p.S + q_start + row;
 #pragma unroll
-                    for (int k = 0; k < 128; ++k)
-                        if (k >= kv_len) s[k] = __float_as_uint(-INFINITY);
-                }
-                float mx = -INFINITY;
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t o[32];
+                    tmem_ld32(taddr + o_cols + cc * 32, o);
+                    tmem_ld_wait();
+                    reg_fence32(o);
+                    if (valid) {
+                        float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D + cc * 32);
 #pragma unroll
-                for (int k = 0; k < 128; ++k) mx = fmaxf(mx, __uint_as_float(s[k]));
-                if (first) {
-                    m_ref = -INFINITY;
-                    l = 0.f;
-                }
-                float alpha = 1.f;
-                bool rescale = false;
-                if (mx > m_ref) {
-                    if (m_ref == -INFINITY) {
-                        m_ref = mx;  // nothing accumulated yet for this row
-                    } else if ((mx - m_ref) * sc > kRescaleThreshold) {
-                        alpha = ex2((m_ref - mx) * sc);
-                        m_ref = mx;
-                        rescale = true;
+                        for (int k = 0; k < 8; ++k)
+                            dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv_l,
+                                                 __uint_as_float(o[4 * k + 1]) * inv_l,
+                                                 __uint_as_float(o[4 * k + 2]) * inv_l,
+                                                 __uint_as_float(o[4 * k + 3]) * inv_l);
                     }
                 }
-                const float neg = -m_ref * sc;
-                float sum = 0.f;
-                uint32_t pk[64];
-#pragma unroll
-                for (int k = 0; k < 64; ++k) {
-                    const float p0 = ex2(fmaf(__uint_as_float(s[2 * k]), sc, neg));
-                    const float p1 = ex2(fmaf(__uint_as_float(s[2 * k + 1]), sc, neg));
-                    sum += p0 + p1;
-                    pk[k] = pack_bf16x2(p0, p1);
-                }
-                tmem_st32(taddr + L::TM_S + st * 128 + 0, pk);
-                tmem_st32(taddr + L::TM_S + st * 128 + 32, pk + 32);
-                l = l * alpha + sum;
-                if (__any_sync(0xffffffffu, rescale)) {
-                    // O holds the product of the tiles before j: wait for the
-                    // last of them (PV_{j-1}) and rescale in place.
-                    if (!(ok = mbar_wait(smem_u32(&bars.o_done), (j - 1) & 1, wc))) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t o[32];
-                        tmem_ld32(taddr + L::TM_O + cc * 32, o);
-                        tmem_ld_wait();
-                        reg_fence32(o);
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                        tmem_st32(taddr + L::TM_O + cc * 32, o);
-                    }
-                }
-                tmem_st_wait();
+                if (valid) p.part_lse[prow] = m_ref * p.scale + logf(l);
                 tc_fence_before();
-                mbar_arrive(smem_u32(&bars.p_full[st]));
-                if (partials && t == t1 - 1) {
-                    // this chunk's partial is complete: O_it / l, LSE_it
-                    if (!(ok = mbar_wait(smem_u32(&bars.o_chunk), it & 1, wc))) break;
-                    tc_fence_after();
-                    const float inv_l = 1.f / l;
-                    const bool valid = row < q_len;
-                    const size_t prow = ((size_t)(it * p.B + b) * p.Hq + h) * p.S + q_start + row;
-#pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t o[32];
-                        tmem_ld32(taddr + L::TM_O + cc * 32, o);
-                        tmem_ld_wait();
-                        reg_fence32(o);
-                        if (valid) {
-                            float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D + cc * 32);
-#pragma unroll
-                            for (int k = 0; k < 8; ++k)
-                                dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv_l,
-                                                     __uint_as_float(o[4 * k + 1]) * inv_l,
-                                                     __uint_as_float(o[4 * k + 2]) * inv_l,
-                                                     __uint_as_float(o[4 * k + 3]) * inv_l);
-                        }
-                    }
-                    if (valid) p.part_lse[prow] = m_ref * p.scale + logf(l);
-                    tc_fence_before();
-                    mbar_arrive(smem_u32(&bars.o_free));
-                }
+                mbar_arrive(smem_u32(&bars.o_free[x]));
             }
         }
         if (ok && !partials) {
             // --------------------------------------------------- epilogue
-            ok = mbar_wait(smem_u32(&bars.o_chunk), 0, wc);
+            ok = mbar_wait(smem_u32(&bars.o_chunk[x]), 0, wc);
             tc_fence_after();
             if (ok) {
                 const float inv_l = 1.f / l;
-                const bool valid = row < q_len;
                 __nv_bfloat16* dst_row =
                     p.out + (int64_t)b * p.o_sb + (int64_t)(q_start + row) * p.o_ss + (int64_t)h * p.o_sh;
 #pragma unroll
                 for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t o[32];
-                    tmem_ld32(taddr + L::TM_O + cc * 32, o);
+                    tmem_ld32(taddr + o_cols + cc * 32, o);
                     tmem_ld_wait();
                     reg_fence32(o);
                     if (valid) {
@@ -359,7 +397,8 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
                                 pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l));
                     }
                 }
-                if (valid) p.lse[((int64_t)b * p.Hq + h) * p.S + q_start + row] = m_ref * p.scale + logf(l);
+                if (valid)
+                    p.lse[((int64_t)b * p.Hq + h) * p.S + q_start + row] = m_ref * p.scale + logf(l);
             }
         }
     }
@@ -376,8 +415,8 @@ int launch_fwd_d(const FwdParams& p, cudaStream_t s) {
     if (cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::SMEM) != cudaSuccess)
         return 4;
-    dim3 grid(p.ct.ntiles, p.Hq, p.B);
-    attn_fwd_kernel<D><<<grid, 192, L::SMEM, s>>>(p);
+    dim3 grid(p.ct.npairs, p.Hq, p.B);
+    attn_fwd_kernel<D><<<grid, kThreads, L::SMEM, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
 

@@ -99,7 +99,11 @@ int build_chunks(int S, int P, const int* offsets, ChunkTable* ct) {
         ct->tile_off[c + 1] = ct->tile_off[c] + (len + kTile - 1) / kTile;
     }
     ct->ntiles = ct->tile_off[P];
-    for (int c = P + 1; c <= kMaxChunks; ++c) ct->off[c] = ct->tile_off[c] = 0;
+    ct->pair_off[0] = 0;
+    for (int c = 0; c < P; ++c)
+        ct->pair_off[c + 1] = ct->pair_off[c] + (ct->tile_off[c + 1] - ct->tile_off[c] + 1) / 2;
+    ct->npairs = ct->pair_off[P];
+    for (int c = P + 1; c <= kMaxChunks; ++c) ct->off[c] = ct->tile_off[c] = ct->pair_off[c] = 0;
     return CTX_OK;
 }
 

@@ -19,8 +19,10 @@ constexpr int kTile = 128;  // rows of a query or key/value tile
 struct ChunkTable {
     int P;
     int ntiles;  // tile_off[P]
+    int npairs;  // pair_off[P]
     int off[kMaxChunks + 1];
     int tile_off[kMaxChunks + 1];
+    int pair_off[kMaxChunks + 1];  // forward CTAs: pairs of consecutive tiles of one chunk
 };
 
 __host__ __device__ inline int chunk_of_tile(const ChunkTable& ct, int t) {
