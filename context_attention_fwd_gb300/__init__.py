@@ -24,10 +24,11 @@ __all__ = [
     "attn_fwd", "attn_bwd", "seq_head_exchange", "exchanged_view", "workspace_size",
     "chunk_offsets", "device_status", "selftest_wait_timeout", "library_path", "load_library",
     "profile_enable", "profile_read",
-    "CtxError", "FLAG_MATERIALIZE_PARTIALS",
+    "CtxError", "FLAG_MATERIALIZE_PARTIALS", "FLAG_KV_ALLGATHER",
 ]
 
 FLAG_MATERIALIZE_PARTIALS = 1
+FLAG_KV_ALLGATHER = 2
 LAYOUT_BSHD, LAYOUT_SBHD = 0, 1
 _lock = threading.Lock()
 _lib = None
@@ -155,7 +156,8 @@ def attn_fwd(q, k, v, P, chunk_offsets=None, causal=False, scale=None, out=None,
     B, S, Hq, D = q.shape
     out = _like_layout(q, Hq) if out is None else out
     lse = torch.empty(B, Hq, S, dtype=torch.float32, device=q.device) if lse is None else lse
-    nbytes = lib.ctx_attn_workspace_size(B, S, Hq, k.shape[2], D, P, flags) if flags else 0
+    nbytes = (lib.ctx_attn_workspace_size(B, S, Hq, k.shape[2], D, P, flags)
+              if flags & FLAG_MATERIALIZE_PARTIALS else 0)
     ws, wsb = _workspace(nbytes, q.device, workspace)
     rc = lib.ctx_attn_fwd(ctypes.byref(_desc(q)), ctypes.byref(_desc(k)), ctypes.byref(_desc(v)), P,
                           _offsets(P, chunk_offsets), LAYOUT_BSHD, int(causal),

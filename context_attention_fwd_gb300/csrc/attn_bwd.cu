@@ -116,7 +116,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     const int kv_start = ct.off[c] + (kt - ct.tile_off[c]) * kTile;
     const int kv_len = min(kTile, ct.off[c + 1] - kv_start);
     const int G = p.group;
-    const int n_q = G * ct.ntiles;
+    int n_q = G * ct.ntiles;  // query tiles this CTA visits (all heads of the group)
+    if (p.causal) {  // chunks after c, and the tiles of chunk c from this KV tile's row on
+        int per = ct.tile_off[c + 1] - ct.tile_off[c] - ((kv_start - ct.off[c]) >> 7);
+        for (int r2 = c + 1; r2 < P; ++r2) per += ct.tile_off[r2 + 1] - ct.tile_off[r2];
+        n_q = G * per;
+    }
     const WaitCtx wc{&bars.abort_flag, p.status, p.timeout_ns};
 
     if (sbase & 1023u) {  // the swizzled tiles need 1024-byte alignment
@@ -150,8 +155,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     tc_fence_after();
     const uint32_t tmem = bars.tmem_slot;
 
-    // advance a query-tile iterator
-    auto next = [&](QTileIter& q) {
+    // query-tile walk: ring order from chunk c; with causal masking, tiles
+    // whose last row precedes this KV tile's first row are skipped (whole
+    // chunks before c, and the head of chunk c)
+    auto q_first_row = [&](const QTileIter& q) { return ct.off[q.r] + (q.t - ct.tile_off[q.r]) * kTile; };
+    auto visible = [&](const QTileIter& q) -> bool {
+        if (!p.causal || q.r > c) return true;
+        if (q.r < c) return false;
+        const int qs = q_first_row(q);
+        return qs + min(kTile, ct.off[q.r + 1] - qs) - 1 >= kv_start;
+    };
+    auto adv = [&](QTileIter& q) {
+        if (p.causal && q.r < c) q.t = ct.tile_off[q.r + 1] - 1;  // the whole chunk is masked
         ++q.t;
         if (q.t == ct.tile_off[q.r + 1]) {
             ++q.it;
@@ -163,11 +178,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             q.t = ct.tile_off[q.r];
         }
     };
+    auto next = [&](QTileIter& q) {
+        do adv(q);
+        while (q.h < hk * G + G && !visible(q));
+    };
     QTileIter q0;
     q0.h = hk * G;
     q0.it = 0;
     q0.r = c;
     q0.t = ct.tile_off[c];
+    while (!visible(q0)) adv(q0);
 
     if (warp == kProducerWarp) {
         // ---------------------------------------------------------- producer
@@ -292,8 +312,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         const float sc = p.scale_log2;
         const bool row_valid = row < kv_len;
         bool ok = true;
-        for (int i = 0; i < n_q; ++i) {
+        QTileIter q = q0;
+        for (int i = 0; i < n_q; ++i, next(q)) {
             const int st = i & 1, ph = (i >> 1) & 1;
+            // causal diagonal tile: query columns before this thread's key are masked
+            const int q_start = q_first_row(q);
+            const bool diag = p.causal && q.r == c && kv_start + kv_len - 1 > q_start;
+            const int lo = diag ? kv_start + row - q_start - half * 64 : 0;  // mask columns k < lo
             const float4* lse2 = reinterpret_cast<const float4*>(stat_base + st * 256 + half * 64);
             const float4* delta = reinterpret_cast<const float4*>(stat_base + st * 256 + 128 + half * 64);
             if (!(ok = mbar_wait(smem_u32(&bars.q_full[st]), ph, wc))) break;
@@ -311,10 +336,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                 const float4 l4 = lse2[k4];
                 const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float pv = ex2(fmaf(__uint_as_float(pr[4 * k4 + e]), sc, -lv[e]));
-                    pr[4 * k4 + e] = __float_as_uint(row_valid ? pv : 0.f);
-                }
+                for (int e = 0; e < 4; ++e)
+                    pr[4 * k4 + e] = __float_as_uint(ex2(fmaf(__uint_as_float(pr[4 * k4 + e]), sc, -lv[e])));
+            }
+            if (diag || kv_len < kTile) {  // tile-uniform: only edge tiles pay for masking
+                const int lo_eff = row_valid ? lo : 64;  // zero columns k < lo_eff
+#pragma unroll
+                for (int k = 0; k < 64; ++k)
+                    if (k < lo_eff) pr[k] = 0u;
             }
             {
                 uint32_t pk[32];

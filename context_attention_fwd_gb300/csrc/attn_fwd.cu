@@ -79,26 +79,43 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
         if (globaltimer_ns() - t0 > limit_ns) break;
 }
 
-// The KV tiles a query chunk r visits, in ring order: iteration it meets
-// chunk (r - it) mod P; tiles [t0, t1) belong to that chunk.
+// The KV tiles the query tiles of chunk r visit.  Ring order: iteration it
+// meets chunk (r - it) mod P; all-gather order: chunk it.  With causal
+// masking, tiles whose first key lies after the CTA's last query row are
+// skipped (whole chunks after r, and the tail of chunk r).
 struct KvWalk {
     int it, c, t, t0, t1;
 };
-__device__ __forceinline__ void kv_first(const ChunkTable& ct, int r, KvWalk& w) {
-    w.it = 0;
-    w.c = r;
-    w.t0 = w.t = ct.tile_off[r];
-    w.t1 = ct.tile_off[r + 1];
+struct WalkCfg {
+    int r, P, causal, allgather, q_last;
+};
+__device__ __forceinline__ void kv_set_chunk(const ChunkTable& ct, const WalkCfg& g, KvWalk& w) {
+    w.c = g.allgather ? w.it : (g.r - w.it + g.P) % g.P;
+    w.t0 = w.t = ct.tile_off[w.c];
+    w.t1 = ct.tile_off[w.c + 1];
 }
-__device__ __forceinline__ void kv_next(const ChunkTable& ct, int r, KvWalk& w) {
-    if (++w.t == w.t1) {
-        ++w.it;
-        if (w.it < ct.P) {
-            w.c = (r - w.it + ct.P) % ct.P;
-            w.t0 = w.t = ct.tile_off[w.c];
-            w.t1 = ct.tile_off[w.c + 1];
-        }
-    }
+__device__ __forceinline__ bool kv_visible(const ChunkTable& ct, const WalkCfg& g, const KvWalk& w) {
+    if (!g.causal || w.c < g.r) return true;
+    if (w.c > g.r) return false;
+    return ct.off[w.c] + (w.t - w.t0) * kTile <= g.q_last;
+}
+__device__ __forceinline__ void kv_adv(const ChunkTable& ct, const WalkCfg& g, KvWalk& w) {
+    if (g.causal && w.c > g.r) w.t = w.t1 - 1;  // the whole chunk is masked
+    if (++w.t == w.t1 && ++w.it < g.P) kv_set_chunk(ct, g, w);
+}
+__device__ __forceinline__ void kv_first(const ChunkTable& ct, const WalkCfg& g, KvWalk& w) {
+    w.it = 0;
+    kv_set_chunk(ct, g, w);
+    while (w.it < g.P && !kv_visible(ct, g, w)) kv_adv(ct, g, w);
+}
+__device__ __forceinline__ void kv_next(const ChunkTable& ct, const WalkCfg& g, KvWalk& w) {
+    do kv_adv(ct, g, w);
+    while (w.it < g.P && !kv_visible(ct, g, w));
+}
+// Number of tiles the walk visits.
+__device__ __forceinline__ int kv_count(const ChunkTable& ct, const WalkCfg& g) {
+    if (!g.causal) return ct.ntiles;
+    return ct.tile_off[g.r] + ((g.q_last - ct.off[g.r]) >> 7) + 1;
 }
 
 template <int D>
@@ -112,7 +129,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t sQ = sbase + L::OFF_Q, sK = sbase + L::OFF_K, sV = sbase + L::OFF_V;
     const int warp = warp_id(), lane = lane_id();
-    const int pair = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // the last pairs carry the most work under causal masking: launch them first
+    const int pair = p.ct.npairs - 1 - (int)blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const ChunkTable& ct = p.ct;
     const int P = ct.P;
     int r = 0;
@@ -122,7 +140,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const int ntile = hasB ? 2 : 1;
     const int qs0 = ct.off[r] + (tA - ct.tile_off[r]) * kTile;
     const int hk = h / p.group;
-    const int n_kv = ct.ntiles;
+    const WalkCfg g{r, P, p.causal, p.allgather,
+                    qs0 + (hasB ? kTile : 0) + min(kTile, ct.off[r + 1] - (qs0 + (hasB ? kTile : 0))) - 1};
+    const int n_kv = kv_count(ct, g);
     const bool partials = p.part_o != nullptr;
     const WaitCtx wc{&abort_flag, p.status, p.timeout_ns};
 
@@ -150,7 +170,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
-
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -165,8 +184,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
             bool ok = true;
             KvWalk w;
-            kv_first(ct, r, w);
-            for (int j = 0; j < n_kv; ++j, kv_next(ct, r, w)) {
+            kv_first(ct, g, w);
+            for (int j = 0; j < n_kv; ++j, kv_next(ct, g, w)) {
                 const int st = j & 1, ph = (j >> 1) & 1;
                 const int kv_start = ct.off[w.c] + (w.t - w.t0) * kTile;
                 if (!(ok = mbar_wait(smem_u32(&bars.k_empty[st]), ph ^ 1, wc))) break;
@@ -208,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             };
             // O_x += P_x V for KV tile j (stage st); first/last: its position in its chunk
             auto issue_pv = [&](int x, int j, int st, bool first, bool last, int it) -> bool {
+                (void)it;
                 if (!mbar_wait(smem_u32(&bars.p_full[x]), j & 1, wc)) return false;
                 if (partials && first && it > 0 && !mbar_wait(smem_u32(&bars.o_free[x]), (it - 1) & 1, wc))
                     return false;
@@ -219,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     mma_ts(tmem + L::TM_O + x * D, tmem + L::TM_S + x * 128 + kk * 8, bdesc, idesc_pv,
                            (acc0 || kk > 0) ? 1u : 0u);
                 }
-                if (last && (partials || it == P - 1)) mma_commit(smem_u32(&bars.o_chunk[x]));
+                if (partials ? last : j == n_kv - 1) mma_commit(smem_u32(&bars.o_chunk[x]));
                 return true;
             };
             bool ok = mbar_wait(smem_u32(&bars.q_full), 0, wc) && mbar_wait(smem_u32(&bars.k_full[0]), 0, wc);
@@ -229,12 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 mma_commit(smem_u32(&bars.k_empty[0]));
             }
             KvWalk w;
-            kv_first(ct, r, w);
+            kv_first(ct, g, w);
             for (int j = 0; j < n_kv && ok; ++j) {
                 const int st = j & 1;
                 const bool first = w.t == w.t0, last = w.t == w.t1 - 1;
                 const int it = w.it;
-                kv_next(ct, r, w);
+                kv_next(ct, g, w);
                 const bool more = j + 1 < n_kv;
                 const int st1 = (j + 1) & 1, ph1 = ((j + 1) >> 1) & 1;
                 if (!(ok = mbar_wait(smem_u32(&bars.v_full[st]), (j >> 1) & 1, wc))) break;
@@ -267,10 +287,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         KvWalk w;
-        kv_first(ct, r, w);
-        for (int j = 0; j < n_kv; ++j, kv_next(ct, r, w)) {
-            const int kv_len = min(kTile, ct.off[w.c + 1] - (ct.off[w.c] + (w.t - w.t0) * kTile));
+        kv_first(ct, g, w);
+        for (int j = 0; j < n_kv; ++j, kv_next(ct, g, w)) {
+            const int kv_start = ct.off[w.c] + (w.t - w.t0) * kTile;
+            const int kv_len = min(kTile, ct.off[w.c + 1] - kv_start);
             const bool first = partials ? (w.t == w.t0) : (j == 0);
+            // keys this row may see in the tile: [0, lim)
+            const bool diag = g.causal && kv_start + kv_len - 1 > q_start;
+            const int lim = diag ? max(0, min(kv_len, q_start + row - kv_start + 1)) : kv_len;
             if (!(ok = mbar_wait(smem_u32(&bars.s_full[x]), j & 1, wc))) break;
             tc_fence_after();
             uint32_t s[128];
@@ -283,10 +307,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             reg_fence32(s + 32);
             reg_fence32(s + 64);
             reg_fence32(s + 96);
-            if (kv_len < kTile) {
+            if (kv_len < kTile || diag) {
 #pragma unroll
                 for (int k = 0; k < 128; ++k)
-                    if (k >= kv_len) s[k] = __float_as_uint(-INFINITY);
+                    if (k >= lim) s[k] = __float_as_uint(-INFINITY);
             }
             float mx8[8];
 #pragma unroll
@@ -312,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     rescale = true;
                 }
             }
-            const float neg = -m_ref * sc;
+            const float neg = m_ref == -INFINITY ? 0.f : -m_ref * sc;  // a row with no key yet
             float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int k = 0; k < 64; ++k) {
@@ -344,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(smem_u32(&bars.p_full[x]));
-            if (partials && w.t == w.t1 - 1) {
+            if (partials && w.t == w.t1 - 1) {  // (no causal masking with partials)
                 // this chunk's partial is complete: O_it / l, LSE_it
                 const int it = w.it;
                 if (!(ok = mbar_wait(smem_u32(&bars.o_chunk[x]), it & 1, wc))) break;

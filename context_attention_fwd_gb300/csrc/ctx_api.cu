@@ -353,13 +353,13 @@ int ctx_attn_fwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
                  int flags, ctx_stream_t stream) {
     if (!q || !k || !v || !out || !lse) return CTX_ERR_INVALID_ARG;
     if (layout != CTX_LAYOUT_BSHD && layout != CTX_LAYOUT_SBHD) return CTX_ERR_INVALID_ARG;
-    if (flags & ~CTX_FLAG_MATERIALIZE_PARTIALS) return CTX_ERR_INVALID_ARG;
+    if (flags & ~(CTX_FLAG_MATERIALIZE_PARTIALS | CTX_FLAG_KV_ALLGATHER)) return CTX_ERR_INVALID_ARG;
     const int64_t B = q->B, S = q->S, Hq = q->H, D = q->D, Hkv = k->H;
     if (B > INT32_MAX || S > INT32_MAX || Hq > 65535 || Hkv > 65535 || B > 65535)
         return CTX_ERR_INVALID_ARG;
     if (!sizes_ok((int)B, (int)S, (int)Hq, (int)Hkv, (int)D)) return CTX_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return CTX_ERR_UNSUPPORTED;
-    if (causal) return CTX_ERR_UNSUPPORTED;
+    if (causal && (flags & CTX_FLAG_MATERIALIZE_PARTIALS)) return CTX_ERR_UNSUPPORTED;
     Dense dq_, dk_, dv_, do_;
     int rc;
     if ((rc = resolve(q, B, S, Hq, D, layout, &dq_))) return rc;
@@ -385,6 +385,8 @@ int ctx_attn_fwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
         return CTX_ERR_CUDA;
     p.B = (int)B; p.S = (int)S; p.Hq = (int)Hq; p.Hkv = (int)Hkv;
     p.group = (int)(Hq / Hkv);
+    p.causal = causal ? 1 : 0;
+    p.allgather = (flags & CTX_FLAG_KV_ALLGATHER) ? 1 : 0;
     p.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
     p.scale_log2 = p.scale * 1.4426950408889634f;
     p.out = static_cast<__nv_bfloat16*>(do_.data);
@@ -421,7 +423,6 @@ int ctx_attn_bwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
         return CTX_ERR_INVALID_ARG;
     if (!sizes_ok((int)B, (int)S, (int)Hq, (int)Hkv, (int)D)) return CTX_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return CTX_ERR_UNSUPPORTED;
-    if (causal) return CTX_ERR_UNSUPPORTED;
     Dense tq, tk, tv, to, tdo, tdq, tdk, tdv;
     int rc;
     if ((rc = resolve(q, B, S, Hq, D, layout, &tq))) return rc;
@@ -452,6 +453,7 @@ int ctx_attn_bwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
         return CTX_ERR_CUDA;
     p.B = (int)B; p.S = (int)S; p.Hq = (int)Hq; p.Hkv = (int)Hkv;
     p.group = (int)(Hq / Hkv);
+    p.causal = causal ? 1 : 0;
     p.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
     p.scale_log2 = p.scale * 1.4426950408889634f;
     p.lse2 = lse2_t;

@@ -35,6 +35,8 @@ struct FwdParams {
     TmaMap tq, tk, tv;
     ChunkTable ct;
     int B, S, Hq, Hkv, group;
+    int causal;        // key j visible to query i iff j <= i (global row indices)
+    int allgather;     // visit KV chunks in order 0..P-1 instead of the ring order
     float scale;       // softmax scale
     float scale_log2;  // scale * log2(e)
     __nv_bfloat16* out;
@@ -52,6 +54,7 @@ struct BwdParams {
     TmaMap tq, tk, tv, tdo;
     ChunkTable ct;
     int B, S, Hq, Hkv, group;
+    int causal;
     float scale, scale_log2;
     // per-row statistics in tile-major order [B][Hq][ntiles][128]:
     const float* lse2;   // lse * log2(e)

@@ -33,7 +33,10 @@
  *    h / (Hq / Hkv) (issue #14265, "How it surfaces": the heads of K/V must
  *    divide the heads of Q).
  *  - Scale: scale <= 0 selects 1/sqrt(D).
- *  - Causal masking is not supported yet (CTX_ERR_UNSUPPORTED).
+ *  - causal != 0: key j is visible to query i iff j <= i (global row
+ *    indices).  KV chunks after a query chunk are skipped entirely, the
+ *    diagonal chunk is masked per element.  The pages' workloads are not
+ *    causal; the definition is the usual one.
  */
 #ifndef CTX_ATTN_H
 #define CTX_ATTN_H
@@ -77,6 +80,11 @@ typedef struct {
  * them with a separate LSE-merge kernel, instead of merging online inside
  * the attention kernel.  Same result up to fp32 rounding order. */
 #define CTX_FLAG_MATERIALIZE_PARTIALS 1
+/* Visit the KV chunks in the order 0..P-1 (the K/V all-gather pattern of
+ * diffusers PR #12443 "Fix Flux Context Parallel Bug ...": every query shard
+ * sees the concatenated K/V) instead of the ring order (r - i) mod P.  Same
+ * result up to fp32 rounding order. */
+#define CTX_FLAG_KV_ALLGATHER 2
 
 /* Bytes of device workspace the calls need for these sizes and flags:
  * max(forward, backward).  Returns 0 on invalid sizes. */
@@ -92,8 +100,9 @@ int ctx_chunk_offsets(int S, int P, int* offsets_out);
  *   out [B,S,Hq,D] (bf16, written), lse [B,Hq,S] fp32 contiguous (written):
  *   lse = natural-log log-sum-exp of the scaled scores over all S keys.
  * P ring chunks (1 <= P <= min(S, 64)).  workspace may be NULL unless
- * CTX_FLAG_MATERIALIZE_PARTIALS is set.  Output rows are written once;
- * out must not alias q, k or v. */
+ * CTX_FLAG_MATERIALIZE_PARTIALS is set (not combined with causal masking:
+ * CTX_ERR_UNSUPPORTED).  Output rows are written once; out must not alias
+ * q, k or v. */
 int ctx_attn_fwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_t* v, int P,
                  const int* chunk_offsets, ctx_layout_t layout, int causal, float scale,
                  const ctx_tensor_t* out, float* lse, void* workspace, size_t workspace_bytes,

@@ -108,11 +108,12 @@ def test_invalid_arguments_fail_before_launch(lib):
     assert call(lse=None) == 1
     assert call(q=_t(fake, 1, 64, 4, 96), k=_t(fake, 1, 64, 2, 96), v=_t(fake, 1, 64, 2, 96),
                 out=_t(fake, 1, 64, 4, 96)) == 2        # D = 96 unsupported
-    assert call(causal=1) == 2                          # causal not implemented yet
+    assert call(causal=1, flags=1) == 2                 # causal with materialised partials
     assert call(out=_t(fake, 1, 63, 4, 64)) == 1        # shape mismatch
     assert call(q=_t(fake + 2, 1, 64, 4, 64)) == 2      # misaligned for TMA
     assert call(flags=1) == 3                           # partials need a workspace
     assert call(flags=4) == 1                           # unknown flag
+    assert call(flags=3) == 3                           # all-gather order + partials: needs a workspace
     offs = (ctypes.c_int * 3)(0, 40, 63)                # must end at S
     assert lib.ctx_attn_fwd(ctypes.byref(q), ctypes.byref(kv), ctypes.byref(kv), 2, offs, 0, 0, 0.0,
                             ctypes.byref(out), lse, None, 0, 0, None) == 1

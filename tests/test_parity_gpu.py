@@ -38,26 +38,26 @@ def check(name, got, ref, tol=TOL):
     return nrm, mx
 
 
-def run_gpu(shape, P=None, offsets=None, flags=0):
+def run_gpu(shape, P=None, offsets=None, flags=0, causal=False):
     q, k, v, do = attn_inputs(shape)
     qd, kd, vd, dod = (t.to("cuda") for t in (q, k, v, do))  # .to() keeps the storage order
     if shape.layout == "sbhd" and shape.B > 1:
         assert qd.stride(1) > qd.stride(0)
     P = shape.P if P is None else P
-    out, lse = ctx.attn_fwd(qd, kd, vd, P, chunk_offsets=offsets, flags=flags)
-    dq, dk, dv = ctx.attn_bwd(qd, kd, vd, out, lse, dod, P, chunk_offsets=offsets)
+    out, lse = ctx.attn_fwd(qd, kd, vd, P, chunk_offsets=offsets, flags=flags, causal=causal)
+    dq, dk, dv = ctx.attn_bwd(qd, kd, vd, out, lse, dod, P, chunk_offsets=offsets, causal=causal)
     torch.cuda.synchronize()
     assert ctx.device_status() == 0
     return (q, k, v, do), (out, lse, dq, dk, dv)
 
 
-def check_full(inputs, outputs):
+def check_full(inputs, outputs, causal=False):
     q, k, v, do = inputs
     out, lse, dq, dk, dv = outputs
-    o_ref, l_ref = oracle.attn_fwd(q, k, v)
+    o_ref, l_ref = oracle.attn_fwd(q, k, v, causal=causal)
     check("out", out, o_ref)
     assert (lse.double().cpu() - l_ref).abs().max() < LSE_TOL
-    dq_r, dk_r, dv_r = oracle.attn_bwd(q, k, v, do)
+    dq_r, dk_r, dv_r = oracle.attn_bwd(q, k, v, do, causal=causal)
     check("dq", dq, dq_r)
     check("dk", dk, dk_r)
     check("dv", dv, dv_r)
@@ -173,6 +173,46 @@ def test_video_s32760_p8_full_size_sampled():
     do_sum = do.float().sum(dim=1).to(dv_sum.device)
     assert ((dv_sum - do_sum).norm() / do_sum.norm()).item() < 2e-2
     assert (dk.float().sum(dim=1).abs().max() / dk.float().abs().sum(dim=1).max()).item() < 2e-2
+
+
+@pytest.mark.parametrize("P", [1, 3, 5])
+@pytest.mark.parametrize("D", [64, 128])
+def test_causal_every_p_gqa(P, D):
+    """Causal masking on global indices: later chunks skipped, diagonal masked."""
+    sh = AttnShape(B=1, S=777, Hq=4, Hkv=2, D=D, P=P)
+    check_full(*run_gpu(sh, causal=True), causal=True)
+
+
+@pytest.mark.parametrize("S,P,layout,offsets", [(1001, 4, "sbhd", None), (130, 1, "bshd", None),
+                                                 (700, 4, "bshd", [0, 1, 300, 429, 700]),
+                                                 (2048, 8, "bshd", None), (5, 5, "bshd", None)])
+def test_causal_layouts_and_edges(S, P, layout, offsets):
+    sh = AttnShape(B=2, S=S, Hq=4, Hkv=4, D=64, P=P, layout=layout)
+    check_full(*run_gpu(sh, offsets=offsets, causal=True), causal=True)
+
+
+def test_causal_partials_refused():
+    sh = AttnShape(B=1, S=256, Hq=2, Hkv=2, D=64, P=2)
+    q, k, v, _ = (t.cuda() for t in attn_inputs(sh))
+    with pytest.raises(ctx.CtxError) as e:
+        ctx.attn_fwd(q, k, v, 2, causal=True, flags=ctx.FLAG_MATERIALIZE_PARTIALS)
+    assert e.value.code == 2
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_kv_allgather_order_matches_ring(causal):
+    """All-gather chunk order (every query shard over the concatenated K/V)
+    computes the same attention as the ring order."""
+    sh = AttnShape(B=1, S=1500, Hq=4, Hkv=2, D=128, P=4)
+    q, k, v, do = attn_inputs(sh)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    o_ring, l_ring = ctx.attn_fwd(qd, kd, vd, 4, causal=causal)
+    o_ag, l_ag = ctx.attn_fwd(qd, kd, vd, 4, causal=causal, flags=ctx.FLAG_KV_ALLGATHER)
+    o_ref, l_ref = oracle.attn_fwd(q, k, v, causal=causal)
+    check("out ring", o_ring, o_ref)
+    check("out allgather", o_ag, o_ref)
+    assert (l_ag.double().cpu() - l_ref).abs().max() < LSE_TOL
+    check("ring vs allgather", o_ag, o_ring, tol=1e-2)
 
 
 def test_timeout_selftest_reports_status():
