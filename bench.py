@@ -41,7 +41,8 @@ L2_NOTE = "inputs larger than L2 (q/k/v/dout 805 MB vs 126.5 MB L2); no flush"
 
 # dram traffic per launch of the backward kernel from one ncu capture (see
 # profiles/); valid only while the kernel source is the one it was taken on.
-NCU_BWD = {"bytes_per_launch": None, "source_sha256": None}
+NCU_BWD = {"bytes_per_launch": 1307783168 + 873230848,  # dram read + write, S=32760 H=24 D=128 P=8
+           "source_sha256": "6e32cc0a3de9943c1768b7c85018e4fd0699242861f55999b529e32b49c98a03"}
 
 
 def flops_fwd(sh: AttnShape) -> float:
@@ -195,6 +196,76 @@ def measure_exchange(ctx, dev, stream, barrier, peaks):
             "bytes": xbytes}
 
 
+def measure_e2e(ctx, dev, sh, host_inputs, ws, steps, barrier, world):
+    """End to end through the public API: every step copies that step's
+    inputs (q, k, v, dout) from pinned host memory to the GPU, runs the
+    forward and backward, and copies the results (out, lse, dq, dk, dv) back
+    to pinned host memory.  Input and output buffers are double-buffered and
+    the copies run on their own streams, so step k's copies overlap the
+    compute of its neighbours, as a pipeline fed with a stream of batches
+    would run; the timed region spans the first input copy to the last
+    result copy.  Returns the e2e dict of the JSON line."""
+    pin = lambda t: t.contiguous().pin_memory()
+    h_in = [pin(t) for t in host_inputs]
+    nbuf = 2
+    d_in = [[torch.empty(t.shape, dtype=t.dtype, device=dev) for t in h_in] for _ in range(nbuf)]
+    oshape = [(sh.B, sh.S, sh.Hq, sh.D), (sh.B, sh.Hq, sh.S), (sh.B, sh.S, sh.Hq, sh.D),
+              (sh.B, sh.S, sh.Hkv, sh.D), (sh.B, sh.S, sh.Hkv, sh.D)]
+    odt = [torch.bfloat16, torch.float32, torch.bfloat16, torch.bfloat16, torch.bfloat16]
+    d_out = [[torch.empty(s_, dtype=t_, device=dev) for s_, t_ in zip(oshape, odt)] for _ in range(nbuf)]
+    h_out = [[torch.empty(s_, dtype=t_, pin_memory=True) for s_, t_ in zip(oshape, odt)] for _ in range(nbuf)]
+    compute = torch.cuda.current_stream(dev)
+    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    in_ready, in_free = [ev() for _ in range(nbuf)], [ev() for _ in range(nbuf)]
+    out_ready, out_free = [ev() for _ in range(nbuf)], [ev() for _ in range(nbuf)]
+
+    def run(k):
+        b = k % nbuf
+        h2d_s.wait_event(in_free[b])  # the compute of step k - 2 has read these inputs
+        with torch.cuda.stream(h2d_s):
+            for d, h in zip(d_in[b], h_in):
+                d.copy_(h, non_blocking=True)
+        in_ready[b].record(h2d_s)
+        compute.wait_event(in_ready[b])
+        compute.wait_event(out_free[b])  # the results of step k - 2 have been copied out
+        q, k_, v, do = d_in[b]
+        out, lse, dq, dk, dv = d_out[b]
+        ctx.attn_fwd(q, k_, v, sh.P, out=out, lse=lse)
+        ctx.attn_bwd(q, k_, v, out, lse, do, sh.P, dq=dq, dk=dk, dv=dv, workspace=ws)
+        in_free[b].record(compute)
+        out_ready[b].record(compute)
+        d2h_s.wait_event(out_ready[b])
+        with torch.cuda.stream(d2h_s):
+            for h, d in zip(h_out[b], d_out[b]):
+                h.copy_(d, non_blocking=True)
+        out_free[b].record(d2h_s)
+
+    for k in range(2):
+        run(k)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(compute)
+    h2d_s.wait_event(e0)
+    for k in range(steps):
+        run(k)
+    compute.wait_event(out_free[(steps - 1) % nbuf])
+    e1.record(compute)
+    barrier()
+    ems = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ems], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ems = t.item()
+    flops_step = flops_fwd(sh) + flops_bwd(sh)
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0])
+    return {"value": world * flops_step * steps / (ems / 1e3) / 1e12, "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems / steps,
+            "overlap": "copies on their own streams, inputs/outputs double-buffered",
+            "gpu_launches": 4 * steps}
+
+
 def source_sha(path):
     with open(path, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()
@@ -294,37 +365,8 @@ def main():
     # ------------------------------------------------ end to end, host buffers
     e2e = None
     if not args.no_e2e:
-        pin = lambda t: t.contiguous().pin_memory()
-        hq, hk, hv, hdo = (pin(t) for t in (q_h, k_h, v_h, do_h))
-        hout, hdq, hdk, hdv = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                               for t in (q_h, q_h, k_h, k_h))
-        hlse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-
-        def e2e_step():
-            for d, h in ((q, hq), (k, hk), (v, hv), (do, hdo)):
-                d.copy_(h, non_blocking=True)
-            step()
-            for h, d in ((hout, out), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
-                h.copy_(d, non_blocking=True)
-
-        for _ in range(2):
-            e2e_step()
-        barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(stream)
-        barrier()
-        ems = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ems = t.item()
-        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
-        d2h = sum(t.numel() * t.element_size() for t in (hout, hlse, hdq, hdk, hdv))
-        e2e = {"value": world * flops_step * args.steps / (ems / 1e3) / 1e12, "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems / args.steps}
+        del out, lse, dq, dk, dv
+        e2e = measure_e2e(ctx, dev, sh, (q_h, k_h, v_h, do_h), ws, args.steps, barrier, world)
 
     # ------------------------------------------------ the exchange (HBM bound)
     exchange = None
@@ -340,7 +382,7 @@ def main():
                         "sustained": 100.0 * value / world / peaks["bf16_sustained"],
                         "peaks_source": peaks["source"]},
         "clocks": clocks,
-        "gpu_launches": 4 * args.steps + (0 if args.no_e2e else 4 * (args.steps + 2)),
+        "gpu_launches": 4 * args.steps,
         "roofline": {"kernel": "attn_bwd_kernel<128>", "bound": "tensor", "achieved": bwd_tf,
                      "peak": peak, "unit": "TFLOP/s", "frac": bwd_tf / peak, "traffic": traffic,
                      "peak_kind": f"bf16 dense, sustained ({peaks['source']})",
