@@ -74,13 +74,14 @@ def load_library(build_if_missing: bool = True):
             lib.ctx_exchange_padded_len.restype = ctypes.c_int64
             lib.ctx_get_device_status.argtypes = [V]
             lib.ctx_selftest_wait_timeout.argtypes = [ctypes.c_uint, V]
+            lib.ctx_selftest_exp2.argtypes = [V, V, V, ctypes.c_int64, V]
             lib.ctx_profile_enable.argtypes = [I]
             lib.ctx_profile_read.argtypes = [I, P(ctypes.c_double), P(I)]
             lib.ctx_status_string.argtypes = [I]
             lib.ctx_status_string.restype = ctypes.c_char_p
             for n in ("ctx_attn_fwd", "ctx_attn_bwd", "ctx_seq_head_exchange", "ctx_chunk_offsets",
                       "ctx_get_device_status", "ctx_selftest_wait_timeout", "ctx_profile_enable",
-                      "ctx_profile_read"):
+                      "ctx_profile_read", "ctx_selftest_exp2"):
                 getattr(lib, n).restype = I
             _lib = lib
     return _lib
@@ -255,6 +256,16 @@ def profile_read(kernel: str):
     _check(load_library().ctx_profile_read(0 if kernel == "fwd" else 1, ctypes.byref(ms), ctypes.byref(n)),
            "ctx_profile_read")
     return ms.value, n.value
+
+
+def selftest_exp2(x: torch.Tensor):
+    """(polynomial 2^x, SFU 2^x) for a CUDA fp32 tensor x, as the kernels compute them."""
+    x = x.contiguous()
+    yp, ys = torch.empty_like(x), torch.empty_like(x)
+    _check(load_library().ctx_selftest_exp2(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(yp.data_ptr()),
+                                            ctypes.c_void_p(ys.data_ptr()), x.numel(), _stream(x)),
+           "ctx_selftest_exp2")
+    return yp, ys
 
 
 def selftest_wait_timeout(timeout_us: int = 20000):

@@ -237,13 +237,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             // Tensor-core order per query tile i: dV_i, dP_i, S_{i+1}, dK_i, dQ_i.
             // P_i is computed while dK_{i-1}, dQ_{i-1} run, dS_i while S_{i+1}
             // runs, and dQ_{i-1} is drained from TMEM while dV_i runs.
+            // Loop-invariant descriptors; a k-step only advances the 14-bit
+            // start-address field (address / 16), which never carries.
+            const uint64_t dK_k = sdesc_sw128(sK, 16, 1024), dV_k = sdesc_sw128(sV, 16, 1024);
+            const uint64_t dQ_k = sdesc_sw128(sQ, 16, 1024), dO_k = sdesc_sw128(sDO, 16, 1024);
+            const uint64_t dQ_mn = sdesc_sw128(sQ, L::BOX, 1024), dO_mn = sdesc_sw128(sDO, L::BOX, 1024);
+            const uint64_t dS_k = sdesc_sw128(sDS, 16, 1024), dS_mn = sdesc_sw128(sDS, L::BOX, 1024);
+            const uint64_t dK_mn = sdesc_sw128(sK, L::BOX, 1024);
+            constexpr uint32_t kStage = L::TILE >> 4, kMnStep = 2048 >> 4;
+            auto koff = [](int kk) -> uint32_t { return ((kk >> 2) * L::BOX + (kk & 3) * 32) >> 4; };
             auto issue_s = [&](int st) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t koff = (kk >> 2) * L::BOX + (kk & 3) * 32;
-                    mma_ss(tmem + L::TM_S, sdesc_sw128(sK + koff, 16, 1024),
-                           sdesc_sw128(sQ + st * L::TILE + koff, 16, 1024), id_st, kk > 0 ? 1u : 0u);
-                }
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + L::TM_S, dK_k + koff(kk), dQ_k + st * kStage + koff(kk), id_st,
+                           kk > 0 ? 1u : 0u);
                 mma_commit(smem_u32(&bars.s_full));
             };
             bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, wc) &&
@@ -261,17 +268,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)
                     mma_ts(tmem + L::TM_DV, tmem + L::TM_S + (kk < 4 ? kk * 8 : 96 + (kk - 4) * 8),
-                           sdesc_sw128(sDOs + kk * 2048, L::BOX, 1024), id_dv,
-                           (i > 0 || kk > 0) ? 1u : 0u);
+                           dO_mn + st * kStage + kk * kMnStep, id_dv, (i > 0 || kk > 0) ? 1u : 0u);
                 // dP^T = V dO^T, into the columns the previous dQ occupied
                 if (i > 0 && !(ok = mbar_wait(smem_u32(&bars.dq_drained), (i - 1) & 1, wc))) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t koff = (kk >> 2) * L::BOX + (kk & 3) * 32;
-                    mma_ss(tmem + L::TM_DP, sdesc_sw128(sV + koff, 16, 1024),
-                           sdesc_sw128(sDOs + koff, 16, 1024), id_st, kk > 0 ? 1u : 0u);
-                }
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + L::TM_DP, dV_k + koff(kk), dO_k + st * kStage + koff(kk), id_st,
+                           kk > 0 ? 1u : 0u);
                 mma_commit(smem_u32(&bars.dp_full));
                 // S^T of the next tile overwrites P^T_i, which dV above has read
                 // (tcgen05.mma from one thread execute in issue order)
@@ -284,16 +288,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                 if (!(ok = mbar_wait(smem_u32(&bars.ds_ready), i & 1, wc))) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk) {
-                    const uint32_t koff = (kk >> 2) * L::BOX + (kk & 3) * 32;
-                    mma_ss(tmem + L::TM_DK, sdesc_sw128(sDS + koff, 16, 1024),
-                           sdesc_sw128(sQs + kk * 2048, L::BOX, 1024), id_dk,
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    mma_ss(tmem + L::TM_DK, dS_k + koff(kk), dQ_mn + st * kStage + kk * kMnStep, id_dk,
                            (i > 0 || kk > 0) ? 1u : 0u);
-                }
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)
-                    mma_ss(tmem + L::TM_DP, sdesc_sw128(sDS + kk * 2048, L::BOX, 1024),
-                           sdesc_sw128(sK + kk * 2048, L::BOX, 1024), id_dq, kk > 0 ? 1u : 0u);
+                    mma_ss(tmem + L::TM_DP, dS_mn + kk * kMnStep, dK_mn + kk * kMnStep, id_dq, kk > 0 ? 1u : 0u);
                 mma_commit(smem_u32(&bars.dq_full));
                 mma_commit(smem_u32(&bars.ds_free));
                 mma_commit(smem_u32(&bars.q_empty[st]));

@@ -118,7 +118,7 @@ __device__ __forceinline__ int kv_count(const ChunkTable& ct, const WalkCfg& g) 
     return ct.tile_off[g.r] + ((g.q_last - ct.off[g.r]) >> 7) + 1;
 }
 
-template <int D>
+template <int D, bool kPartials>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
     using L = FwdLayout<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const WalkCfg g{r, P, p.causal, p.allgather,
                     qs0 + (hasB ? kTile : 0) + min(kTile, ct.off[r + 1] - (qs0 + (hasB ? kTile : 0))) - 1};
     const int n_kv = kv_count(ct, g);
-    const bool partials = p.part_o != nullptr;
+    constexpr bool partials = kPartials;
     const WaitCtx wc{&abort_flag, p.status, p.timeout_ns};
 
     if (threadIdx.x == 0) {
@@ -215,13 +215,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
+            // Loop-invariant descriptors; a k-step only advances the 14-bit
+            // start-address field (address / 16), which never carries.
+            const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024), dk0 = sdesc_sw128(sK, 16, 1024);
+            const uint64_t dv0 = sdesc_sw128(sV, L::BOX, 1024);
             // S_x = Q_x K^T for the K tile in stage st
             auto issue_s = [&](int x, int st) {
+                const uint64_t a = dq0 + ((x * L::TILE) >> 4), bq = dk0 + ((st * L::TILE) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t koff = (kk >> 2) * L::BOX + (kk & 3) * 32;
-                    mma_ss(tmem + L::TM_S + x * 128, sdesc_sw128(sQ + x * L::TILE + koff, 16, 1024),
-                           sdesc_sw128(sK + st * L::TILE + koff, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                    const uint32_t koff = ((kk >> 2) * L::BOX + (kk & 3) * 32) >> 4;
+                    mma_ss(tmem + L::TM_S + x * 128, a + koff, bq + koff, idesc_qk, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(smem_u32(&bars.s_full[x]));
             };
@@ -233,12 +237,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     return false;
                 tc_fence_after();
                 const bool acc0 = partials ? !first : j > 0;
+                const uint64_t bv = dv0 + ((st * L::TILE) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk) {
-                    const uint64_t bdesc = sdesc_sw128(sV + st * L::TILE + kk * 2048, L::BOX, 1024);
-                    mma_ts(tmem + L::TM_O + x * D, tmem + L::TM_S + x * 128 + kk * 8, bdesc, idesc_pv,
-                           (acc0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    mma_ts(tmem + L::TM_O + x * D, tmem + L::TM_S + x * 128 + kk * 8, bv + kk * (2048 >> 4),
+                           idesc_pv, (acc0 || kk > 0) ? 1u : 0u);
                 if (partials ? last : j == n_kv - 1) mma_commit(smem_u32(&bars.o_chunk[x]));
                 return true;
             };
@@ -433,15 +436,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     if (warp == 1) tmem_dealloc(tmem, L::TM_COLS);
 }
 
-template <int D>
-int launch_fwd_d(const FwdParams& p, cudaStream_t s) {
+template <int D, bool kPartials>
+int launch_fwd_dp(const FwdParams& p, cudaStream_t s) {
     using L = FwdLayout<D>;
-    if (cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attn_fwd_kernel<D, kPartials>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::SMEM) != cudaSuccess)
         return 4;
     dim3 grid(p.ct.npairs, p.Hq, p.B);
-    attn_fwd_kernel<D><<<grid, kThreads, L::SMEM, s>>>(p);
+    attn_fwd_kernel<D, kPartials><<<grid, kThreads, L::SMEM, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+// The materialised-partials code path is a separate instantiation so that
+// the default online kernel carries none of its registers.
+template <int D>
+int launch_fwd_d(const FwdParams& p, cudaStream_t s) {
+    return p.part_o ? launch_fwd_dp<D, true>(p, s) : launch_fwd_dp<D, false>(p, s);
 }
 
 }  // namespace

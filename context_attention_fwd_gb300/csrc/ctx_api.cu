@@ -254,6 +254,16 @@ __global__ void lse_merge_kernel(const float* __restrict__ part_o, const float* 
     if (k4 == 0) lse[row] = L;
 }
 
+// Self test of the two exponentials the attention kernels use.
+__global__ void exp2_selftest_kernel(const float* __restrict__ x, float* __restrict__ y_poly,
+                                     float* __restrict__ y_sfu, int64_t n) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) {
+        y_poly[i] = ex2_poly(x[i]);
+        y_sfu[i] = ex2(x[i]);
+    }
+}
+
 // Failure-detection self test: wait on an mbarrier nothing arrives on.
 __global__ void wait_timeout_kernel(int* status, uint64_t limit_ns) {
     __shared__ uint64_t bar;
@@ -591,6 +601,13 @@ int ctx_profile_read(int kernel, double* total_ms, int* launches) {
     *total_ms = sum;
     *launches = g_prof.n[kernel];
     return CTX_OK;
+}
+
+int ctx_selftest_exp2(const float* x, float* y_poly, float* y_sfu, int64_t n, ctx_stream_t stream) {
+    if (!x || !y_poly || !y_sfu || n < 1 || n > ((int64_t)1 << 31)) return CTX_ERR_INVALID_ARG;
+    exp2_selftest_kernel<<<(unsigned)((n + 255) / 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        x, y_poly, y_sfu, n);
+    return launch_status();
 }
 
 int ctx_selftest_wait_timeout(unsigned timeout_us, ctx_stream_t stream) {

@@ -181,6 +181,12 @@ int ctx_get_device_status(ctx_stream_t stream);
  * status word and returns.  Nothing faults or hangs. */
 int ctx_selftest_wait_timeout(unsigned timeout_us, ctx_stream_t stream);
 
+/* Self test of the exponentials inside the attention kernels: for n inputs
+ * x (device fp32), writes 2^x computed by the polynomial the kernels run on
+ * the FMA pipe (y_poly) and by the SFU instruction (y_sfu), so that a test can
+ * hold both against a reference exp2.  Device buffers, n <= 2^31. */
+int ctx_selftest_exp2(const float* x, float* y_poly, float* y_sfu, int64_t n, ctx_stream_t stream);
+
 /* Kernel timing for measurement.  While enabled, every launch of the
  * attention forward kernel (kernel 0) and backward kernel (kernel 1) is
  * bracketed by a pair of CUDA events recorded on the launch stream (at most

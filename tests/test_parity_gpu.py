@@ -215,6 +215,22 @@ def test_kv_allgather_order_matches_ring(causal):
     check("ring vs allgather", o_ag, o_ring, tol=1e-2)
 
 
+def test_exp2_polynomial_and_sfu_accuracy():
+    """The two exponentials the kernels use, against torch's exp2 in fp64:
+    the FMA-pipe polynomial within its 7.5e-5 design bound (plus fp32
+    rounding), the SFU within 2^-20 relative; both far below bf16's 3.9e-3."""
+    x = torch.cat([torch.linspace(-125.0, 8.0, 1 << 20), torch.linspace(-1.0, 1.0, 1 << 16)]).cuda()
+    yp, ys = ctx.selftest_exp2(x)
+    ref = torch.exp2(x.double())
+    rel_p = ((yp.double() - ref).abs() / ref).max().item()
+    rel_s = ((ys.double() - ref).abs() / ref).max().item()
+    assert rel_p < 1e-4, rel_p
+    assert rel_s < 2 ** -20, rel_s
+    # below the clamp the polynomial returns 2^-125, a negligible weight
+    yp2, _ = ctx.selftest_exp2(torch.tensor([-126.0, -500.0, float("-inf")], device="cuda"))
+    assert (yp2.double() <= 2.0 ** -124).all() and (yp2 > 0).all()
+
+
 def test_timeout_selftest_reports_status():
     """A device wait that nothing satisfies gives up and reports CTX_ERR_TIMEOUT."""
     assert ctx.device_status() == 0
