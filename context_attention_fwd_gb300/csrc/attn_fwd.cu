@@ -18,14 +18,19 @@
 //
 // Warp roles (384 threads):
 //   warp 0       TMA producer: Q_A, Q_B once, K/V tiles through a 2-stage ring
-//   warp 1       TMEM owner and tcgen05.mma issuer (one elected lane)
+//   warp 1       TMEM owner
 //   warps 2, 3   idle (keep the softmax warpgroups warpgroup-aligned)
-//   warps 4..7   softmax of tile A, warps 8..11 softmax of tile B: one query
-//                row per thread, S from TMEM, P back to TMEM as bf16 (A
-//                operand of the PV product), lazy O rescale, epilogue
+//   warps 4..7   tile A, warps 8..11 tile B: one query row per thread; S from
+//                TMEM, mask, max, exp2, sum, P back to TMEM as bf16 (the A
+//                operand of the PV product), lazy O rescale, epilogue.  Lane 0
+//                of the first warp of each group issues that tile's own
+//                tcgen05.mma: PV_x(j) then S_x(j+1), so each tile is an
+//                independent pipeline and the tensor core is fed by two
+//                issuers: while one waits on a barrier, the other's queued
+//                products keep it busy.
 // TMEM (512 columns): S_A 0, S_B 128, O_A 256, O_B 256 + D.
-// Tensor-core order: S_A(j) S_B(j) PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) ...
-// so each softmax overlaps two products of the other tile.
+// S_x = Q_x K^T: A = Q (smem, K-major), B = K (smem, K-major), M=N=128.
+// O_x += P_x V:  A = P (TMEM), B = V (smem, MN-major: V rows are the K index).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -50,17 +55,21 @@ struct FwdLayout {
 
 struct FwdBars {
     uint64_t q_full;
-    uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
-    uint64_t s_full[2], p_full[2];  // per query tile
-    uint64_t o_chunk[2];  // per tile: after the last PV of a chunk (every chunk with partials, else once)
-    uint64_t o_free[2];   // partials: O drained, the next chunk may overwrite it
-    uint64_t drain;       // teardown: all MMAs retired
+    uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];  // empties: one commit per tile issuer
+    uint64_t s_done[2];   // per tile: S_x(j) computed
+    uint64_t o_done[2];   // per tile: the last PV of a chunk (partials) or of the walk computed
+    uint64_t drain[2];    // per tile issuer, teardown: all its MMAs retired
 };
 
 constexpr int kThreads = 384;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kSoftmaxWarp0 = 4;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: move the reference max lazily
+
+// Barrier among the 128 threads of one softmax warpgroup (ids 1 and 2).
+__device__ __forceinline__ void group_sync(int id) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kSoftmaxThreads) : "memory");
+}
 
 __device__ __forceinline__ int pick3(int o, int s, int h, int b) {
     return o == 0 ? s : (o == 1 ? h : b);
@@ -151,15 +160,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         mbar_init(smem_u32(&bars.q_full), 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&bars.k_full[i]), 1);
-            mbar_init(smem_u32(&bars.k_empty[i]), 1);
+            mbar_init(smem_u32(&bars.k_empty[i]), ntile);
             mbar_init(smem_u32(&bars.v_full[i]), 1);
-            mbar_init(smem_u32(&bars.v_empty[i]), 1);
-            mbar_init(smem_u32(&bars.s_full[i]), 1);
-            mbar_init(smem_u32(&bars.p_full[i]), kSoftmaxThreads);
-            mbar_init(smem_u32(&bars.o_chunk[i]), 1);
-            mbar_init(smem_u32(&bars.o_free[i]), kSoftmaxThreads);
+            mbar_init(smem_u32(&bars.v_empty[i]), ntile);
+            mbar_init(smem_u32(&bars.s_done[i]), 1);
+            mbar_init(smem_u32(&bars.o_done[i]), 1);
+            mbar_init(smem_u32(&bars.drain[i]), 1);
         }
-        mbar_init(smem_u32(&bars.drain), 1);
         mbar_fence_init();
     }
     if (warp == 1) {
@@ -210,95 +217,51 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 }
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
-            // Loop-invariant descriptors; a k-step only advances the 14-bit
-            // start-address field (address / 16), which never carries.
-            const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024), dk0 = sdesc_sw128(sK, 16, 1024);
-            const uint64_t dv0 = sdesc_sw128(sV, L::BOX, 1024);
-            // S_x = Q_x K^T for the K tile in stage st
-            auto issue_s = [&](int x, int st) {
-                const uint64_t a = dq0 + ((x * L::TILE) >> 4), bq = dk0 + ((st * L::TILE) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t koff = ((kk >> 2) * L::BOX + (kk & 3) * 32) >> 4;
-                    mma_ss(tmem + L::TM_S + x * 128, a + koff, bq + koff, idesc_qk, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(smem_u32(&bars.s_full[x]));
-            };
-            // O_x += P_x V for KV tile j (stage st); first/last: its position in its chunk
-            auto issue_pv = [&](int x, int j, int st, bool first, bool last, int it) -> bool {
-                (void)it;
-                if (!mbar_wait(smem_u32(&bars.p_full[x]), j & 1, wc)) return false;
-                if (partials && first && it > 0 && !mbar_wait(smem_u32(&bars.o_free[x]), (it - 1) & 1, wc))
-                    return false;
-                tc_fence_after();
-                const bool acc0 = partials ? !first : j > 0;
-                const uint64_t bv = dv0 + ((st * L::TILE) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)
-                    mma_ts(tmem + L::TM_O + x * D, tmem + L::TM_S + x * 128 + kk * 8, bv + kk * (2048 >> 4),
-                           idesc_pv, (acc0 || kk > 0) ? 1u : 0u);
-                if (partials ? last : j == n_kv - 1) mma_commit(smem_u32(&bars.o_chunk[x]));
-                return true;
-            };
-            bool ok = mbar_wait(smem_u32(&bars.q_full), 0, wc) && mbar_wait(smem_u32(&bars.k_full[0]), 0, wc);
-            if (ok) {
-                tc_fence_after();
-                for (int x = 0; x < ntile; ++x) issue_s(x, 0);
-                mma_commit(smem_u32(&bars.k_empty[0]));
-            }
-            KvWalk w;
-            kv_first(ct, g, w);
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int st = j & 1;
-                const bool first = w.t == w.t0, last = w.t == w.t1 - 1;
-                const int it = w.it;
-                kv_next(ct, g, w);
-                const bool more = j + 1 < n_kv;
-                const int st1 = (j + 1) & 1, ph1 = ((j + 1) >> 1) & 1;
-                if (!(ok = mbar_wait(smem_u32(&bars.v_full[st]), (j >> 1) & 1, wc))) break;
-                if (!(ok = issue_pv(0, j, st, first, last, it))) break;
-                if (more) {  // S_A(j+1) overwrites P_A(j): issued after PV_A(j), executed in order
-                    if (!(ok = mbar_wait(smem_u32(&bars.k_full[st1]), ph1, wc))) break;
-                    tc_fence_after();
-                    issue_s(0, st1);
-                }
-                if (hasB && !(ok = issue_pv(1, j, st, first, last, it))) break;
-                mma_commit(smem_u32(&bars.v_empty[st]));
-                if (more) {
-                    if (hasB) issue_s(1, st1);
-                    mma_commit(smem_u32(&bars.k_empty[st1]));
-                }
-            }
-            mma_commit(smem_u32(&bars.drain));
-            drain_wait(smem_u32(&bars.drain), 0, p.timeout_ns);
-        }
     } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4 * ntile) {
-        // ------------------------------------------------------ softmax
+        // ------------------------------------------------------ softmax + MMA issue of tile x
         const int x = (warp - kSoftmaxWarp0) >> 2;  // query tile A (0) or B (1)
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
+        const bool issuer = (warp & 3) == 0 && lane == 0;
         const uint32_t taddr = tmem + (uint32_t(quarter * 32) << 16);
         const uint32_t s_cols = L::TM_S + x * 128, o_cols = L::TM_O + x * D;
         const int q_start = qs0 + x * kTile;
         const float sc = p.scale_log2;
         const bool valid = row < ct.off[r + 1] - q_start;
-        float m_ref = -INFINITY, l = 0.f;
+        constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
+        // Loop-invariant descriptors; a k-step only advances the 14-bit
+        // start-address field (address / 16), which never carries.
+        const uint64_t dq0 = sdesc_sw128(sQ + x * L::TILE, 16, 1024), dk0 = sdesc_sw128(sK, 16, 1024);
+        const uint64_t dv0 = sdesc_sw128(sV, L::BOX, 1024);
+        const uint32_t s_done = smem_u32(&bars.s_done[x]), o_done = smem_u32(&bars.o_done[x]);
+        auto issue_s = [&](int st) {  // S_x = Q_x K^T, K tile in stage st
+            const uint64_t bk = dk0 + ((st * L::TILE) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t koff = ((kk >> 2) * L::BOX + (kk & 3) * 32) >> 4;
+                mma_ss(tmem + s_cols, dq0 + koff, bk + koff, idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(s_done);
+            mma_commit(smem_u32(&bars.k_empty[st]));
+        };
         bool ok = true;
+        if (issuer) {
+            ok = mbar_wait(smem_u32(&bars.q_full), 0, wc) && mbar_wait(smem_u32(&bars.k_full[0]), 0, wc);
+            if (ok) issue_s(0);
+        }
+        __syncwarp();  // park the issuer's warp-mates instead of letting them spin
+        float m_ref = -INFINITY, l = 0.f;
         KvWalk w;
         kv_first(ct, g, w);
-        for (int j = 0; j < n_kv; ++j, kv_next(ct, g, w)) {
+        for (int j = 0; j < n_kv && ok; ++j, kv_next(ct, g, w)) {
             const int kv_start = ct.off[w.c] + (w.t - w.t0) * kTile;
             const int kv_len = min(kTile, ct.off[w.c + 1] - kv_start);
             const bool first = partials ? (w.t == w.t0) : (j == 0);
             // keys this row may see in the tile: [0, lim)
             const bool diag = g.causal && kv_start + kv_len - 1 > q_start;
             const int lim = diag ? max(0, min(kv_len, q_start + row - kv_start + 1)) : kv_len;
-            if (!(ok = mbar_wait(smem_u32(&bars.s_full[x]), j & 1, wc))) break;
+            if (!(ok = mbar_wait(s_done, j & 1, wc))) break;
             tc_fence_after();
             uint32_t s[128];
             tmem_ld32(taddr + s_cols + 0, s);
@@ -355,8 +318,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                               ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
             l = l * alpha + sum;
             if (__any_sync(0xffffffffu, rescale)) {
-                // PV of the previous KV tile was issued before this S and has
-                // completed with it: rescale O in place.
+                // PV of the previous KV tile was issued before this S (same
+                // issuer) and has completed with it: rescale O in place.
 #pragma unroll
                 for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t o[32];
@@ -370,11 +333,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(smem_u32(&bars.p_full[x]));
-            if (partials && w.t == w.t1 - 1) {  // (no causal masking with partials)
+            group_sync(1 + x);  // every P (and O rescale) of this tile is in TMEM
+            const bool first_c = w.t == w.t0, last_c = w.t == w.t1 - 1;
+            if (issuer) {
+                tc_fence_after();
+                const int st = j & 1, st1 = (j + 1) & 1;
+                // O_x += P_x V: V tile of stage st
+                if (!(ok = mbar_wait(smem_u32(&bars.v_full[st]), (j >> 1) & 1, wc))) {
+                    *wc.abort_flag = 1;
+                } else {
+                    const bool acc0 = partials ? !first_c : j > 0;
+                    const uint64_t bv = dv0 + ((st * L::TILE) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        mma_ts(tmem + o_cols, tmem + s_cols + kk * 8, bv + kk * (2048 >> 4), idesc_pv,
+                               (acc0 || kk > 0) ? 1u : 0u);
+                    mma_commit(smem_u32(&bars.v_empty[st]));
+                    if (partials ? last_c : j == n_kv - 1) mma_commit(o_done);
+                    // S_x(j+1) overwrites P_x(j): issued after the PV that reads it (in order)
+                    if (j + 1 < n_kv) {
+                        if (mbar_wait(smem_u32(&bars.k_full[st1]), ((j + 1) >> 1) & 1, wc))
+                            issue_s(st1);
+                        else
+                            *wc.abort_flag = 1;
+                    }
+                }
+            }
+            __syncwarp();
+            if (partials && last_c) {  // (no causal masking with partials)
                 // this chunk's partial is complete: O_it / l, LSE_it
                 const int it = w.it;
-                if (!(ok = mbar_wait(smem_u32(&bars.o_chunk[x]), it & 1, wc))) break;
+                if (!(ok = mbar_wait(o_done, it & 1, wc))) break;
                 tc_fence_after();
                 const float inv_l = 1.f / l;
                 const size_t prow = ((size_t)(it * p.B + b) * p.Hq + h) * p.S + q_start + row;
@@ -395,13 +384,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     }
                 }
                 if (valid) p.part_lse[prow] = m_ref * p.scale + logf(l);
-                tc_fence_before();
-                mbar_arrive(smem_u32(&bars.o_free[x]));
+                tc_fence_before();  // the next chunk's first PV overwrites O after the next group_sync
             }
         }
         if (ok && !partials) {
             // --------------------------------------------------- epilogue
-            ok = mbar_wait(smem_u32(&bars.o_chunk[x]), 0, wc);
+            ok = mbar_wait(o_done, 0, wc);
             tc_fence_after();
             if (ok) {
                 const float inv_l = 1.f / l;
@@ -430,6 +418,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
     }
 
+    if (warp >= kSoftmaxWarp0 && (warp & 3) == 0 && lane == 0 && warp < kSoftmaxWarp0 + 4 * ntile) {
+        const int x = (warp - kSoftmaxWarp0) >> 2;  // this tile's issued MMAs must retire first
+        mma_commit(smem_u32(&bars.drain[x]));
+        drain_wait(smem_u32(&bars.drain[x]), 0, p.timeout_ns);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

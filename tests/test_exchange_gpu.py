@@ -101,3 +101,48 @@ def test_hybrid_ring_x_ulysses_matches_plain_ring(S):
     check("dk", dk_h, g_ref[1])
     check("dv", dv_h, g_ref[2])
     assert ctx.device_status() == 0
+
+
+def test_head_group_views_read_the_unexchanged_layout():
+    """Fused exchange + attention: a head group's attention reads the
+    pre-exchange tensor through a strided view (no copy) and gives bit for
+    bit what it gives on the exchanged buffer."""
+    sh = AttnShape(B=1, S=2000, Hq=8, Hkv=4, D=128, P=4)
+    q, k, v, _ = (t.cuda() for t in attn_inputs(sh))
+    ring, U = 4, 2
+    Hu, Hku = sh.Hq // U, sh.Hkv // U
+    ex = lambda t: ctx.seq_head_exchange(t, ring, U, 0, "bshd")
+    yq, yk, yv = ex(q), ex(k), ex(v)
+    for u in range(U):
+        o_view, l_view = ctx.attn_fwd(q[:, :, u * Hu:(u + 1) * Hu], k[:, :, u * Hku:(u + 1) * Hku],
+                                      v[:, :, u * Hku:(u + 1) * Hku], ring)
+        o_ex, l_ex = ctx.attn_fwd(yq[u][:, :sh.S], yk[u][:, :sh.S], yv[u][:, :sh.S], ring)
+        assert torch.equal(bits(o_view), bits(o_ex))
+        assert torch.equal(l_view.cpu(), l_ex.cpu())
+
+
+def test_hybrid_ring4_ulysses2_full_size_sampled():
+    """The ring 4 x ulysses 2 hybrid at full size: exchange of
+    [1,65536,32,128] (k, v with 8 heads), GQA 32/8 attention over 4 ring
+    chunks on the exchanged tensors, inverse exchange; forward and backward.
+    Sampled rows against the oracle; dk/dv through the sum rules."""
+    from test_parity_gpu import check
+    sh = HYBRID_S65536
+    q, k, v, do = attn_inputs(sh)
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    out, dq, dk, dv, offs = hybrid(qd, kd, vd, dod, ring=HYBRID_RING, U=HYBRID_ULYSSES)
+    torch.cuda.synchronize()
+    assert ctx.device_status() == 0
+    g = torch.Generator().manual_seed(2)
+    rows = [(0, int(h), int(s)) for h, s in zip(torch.randint(0, sh.Hq, (24,), generator=g),
+                                                torch.randint(0, sh.S, (24,), generator=g))]
+    rows += [(0, 17, s) for s in (0, 16383, 16384, 32767, 32768, 49152, 65535)]  # rank edges
+    o_ref, _ = oracle.fwd_rows(q, k, v, rows)
+    check("out rows", torch.stack([out[b, s, h].cpu() for b, h, s in rows]), o_ref)
+    dq_ref = oracle.dq_rows(q, k, v, do, rows[:16])
+    check("dq rows", torch.stack([dq[b, s, h].cpu() for b, h, s in rows[:16]]), dq_ref)
+    G = sh.Hq // sh.Hkv
+    do_grp = do.float().reshape(sh.B, sh.S, sh.Hkv, G, sh.D).sum(dim=(1, 3)).to(dv.device)
+    dv_sum = dv.float().sum(dim=1)
+    assert ((dv_sum - do_grp).norm() / do_grp.norm()).item() < 2e-2
+    assert (dk.float().sum(dim=1).abs().max() / dk.float().abs().sum(dim=1).max()).item() < 2e-2
