@@ -22,13 +22,18 @@
 // dQ tiles are added into an fp32 accumulator in global memory (vector
 // reductions); dK, dV stay in TMEM for the whole CTA and are written once.
 //
-// Warp roles (448 threads):
+// Warp roles (480 threads):
 //   warps 0..7   P / dS math: one KV row per thread (TMEM lane quarter =
 //                warp mod 4), warps 0..3 take query columns 0..63 and warps
 //                4..7 columns 64..127; dV epilogue (half the columns each)
 //   warps 8..11  dQ drain (one query row per thread); dK epilogue
 //   warp 12      TMA producer (K, V once; Q, dO, lse, delta per query tile, 2 stages)
-//   warp 13      TMEM owner and MMA issuer
+//   warp 13      TMEM owner; issues S and dP (the products that feed the math)
+//   warp 14      issues dV, dK and dQ (the products that consume the math)
+// Two MMA issuers keep the tensor core fed: while one waits on a barrier,
+// the products the other has queued keep running.  Their TMEM hazards are
+// ordered explicitly: S_{i+1} waits until dV_i (which reads P^T_i from the S
+// columns) is done, dP_{i+1} until dQ_i (written over dP_i) has been drained.
 // P^T is written back into the S^T columns it was computed from (bf16
 // pairs): columns 0..31 for query columns 0..63, columns 96..127 for query
 // columns 64..127, so the two math warps of a lane quarter never overwrite
@@ -59,10 +64,10 @@ struct BwdLayout {
 struct BwdBars {
     uint64_t kv_full;
     uint64_t q_full[2], q_empty[2];
-    uint64_t s_full, dp_full, p_ready, ds_ready, ds_free;
+    uint64_t s_full, dp_full, p_ready, ds_ready, ds_free, dv_done;
     uint64_t dq_full, dq_drained;
     uint64_t final_mma;
-    uint64_t drain;
+    uint64_t drain, drain2;
     uint32_t tmem_slot;
     int abort_flag;
 };
@@ -70,8 +75,8 @@ struct BwdBars {
 constexpr int kMathWarps = 8;
 constexpr int kMathThreads = 32 * kMathWarps;
 constexpr int kDrainThreads = 128;
-constexpr int kThreads = 448;
-constexpr int kProducerWarp = 12, kMmaWarp = 13;
+constexpr int kThreads = 480;
+constexpr int kProducerWarp = 12, kMmaWarp = 13, kMma2Warp = 14;
 
 __device__ __forceinline__ int pick3(int o, int s, int h, int b) {
     return o == 0 ? s : (o == 1 ? h : b);
@@ -140,6 +145,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         mbar_init(smem_u32(&bars.p_ready), kMathThreads);
         mbar_init(smem_u32(&bars.ds_ready), kMathThreads);
         mbar_init(smem_u32(&bars.ds_free), 1);
+        mbar_init(smem_u32(&bars.dv_done), 1);
+        mbar_init(smem_u32(&bars.drain2), 1);
         mbar_init(smem_u32(&bars.dq_full), 1);
         mbar_init(smem_u32(&bars.dq_drained), kDrainThreads);
         mbar_init(smem_u32(&bars.final_mma), 1);
@@ -227,16 +234,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                     if (last_ph[st] >= 0) drain_wait(smem_u32(&bars.q_full[st]), last_ph[st], p.timeout_ns);
             }
         }
-    } else if (warp == kMmaWarp) {
-        // ---------------------------------------------------------- MMA issuer
+    } else if (warp == kMmaWarp || warp == kMma2Warp) {
+        // ---------------------------------------------------------- MMA issuers
         if (lane == 0) {
             constexpr uint32_t id_st = idesc_bf16_f32(128, 128, false, false);  // K-major A and B
             constexpr uint32_t id_dv = idesc_bf16_f32(128, D, false, true);     // A TMEM, B MN-major
             constexpr uint32_t id_dk = idesc_bf16_f32(128, D, false, true);     // A K-major smem, B MN-major
             constexpr uint32_t id_dq = idesc_bf16_f32(128, D, true, true);      // A MN-major, B MN-major
-            // Tensor-core order per query tile i: dV_i, dP_i, S_{i+1}, dK_i, dQ_i.
-            // P_i is computed while dK_{i-1}, dQ_{i-1} run, dS_i while S_{i+1}
-            // runs, and dQ_{i-1} is drained from TMEM while dV_i runs.
             // Loop-invariant descriptors; a k-step only advances the 14-bit
             // start-address field (address / 16), which never carries.
             const uint64_t dK_k = sdesc_sw128(sK, 16, 1024), dV_k = sdesc_sw128(sV, 16, 1024);
@@ -246,61 +250,64 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             const uint64_t dK_mn = sdesc_sw128(sK, L::BOX, 1024);
             constexpr uint32_t kStage = L::TILE >> 4, kMnStep = 2048 >> 4;
             auto koff = [](int kk) -> uint32_t { return ((kk >> 2) * L::BOX + (kk & 3) * 32) >> 4; };
-            auto issue_s = [&](int st) {
+            bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, wc);
+            if (warp == kMmaWarp) {
+                // S_i = K Q_i^T and dP_i = V dO_i^T, per query tile
+                auto issue_s = [&](int st) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + L::TM_S, dK_k + koff(kk), dQ_k + st * kStage + koff(kk), id_st,
-                           kk > 0 ? 1u : 0u);
-                mma_commit(smem_u32(&bars.s_full));
-            };
-            bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, wc) &&
-                      mbar_wait(smem_u32(&bars.q_full[0]), 0, wc);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0);  // S^T_0 = K Q_0^T
-            }
-            for (int i = 0; i < n_q && ok; ++i) {
-                const int st = i & 1;
-                const uint32_t sQs = sQ + st * L::TILE, sDOs = sDO + st * L::TILE;
-                // dV += P^T dO
-                if (!(ok = mbar_wait(smem_u32(&bars.p_ready), i & 1, wc))) break;
-                tc_fence_after();
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + L::TM_S, dK_k + koff(kk), dQ_k + st * kStage + koff(kk), id_st,
+                               kk > 0 ? 1u : 0u);
+                    mma_commit(smem_u32(&bars.s_full));
+                };
+                if (ok && (ok = mbar_wait(smem_u32(&bars.q_full[0]), 0, wc))) issue_s(0);
+                for (int i = 0; i < n_q && ok; ++i) {
+                    const int st = i & 1;
+                    // dP^T = V dO^T, into the columns dQ_{i-1} occupied once it is drained
+                    if (i > 0 && !(ok = mbar_wait(smem_u32(&bars.dq_drained), (i - 1) & 1, wc))) break;
 #pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)
-                    mma_ts(tmem + L::TM_DV, tmem + L::TM_S + (kk < 4 ? kk * 8 : 96 + (kk - 4) * 8),
-                           dO_mn + st * kStage + kk * kMnStep, id_dv, (i > 0 || kk > 0) ? 1u : 0u);
-                // dP^T = V dO^T, into the columns the previous dQ occupied
-                if (i > 0 && !(ok = mbar_wait(smem_u32(&bars.dq_drained), (i - 1) & 1, wc))) break;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + L::TM_DP, dV_k + koff(kk), dO_k + st * kStage + koff(kk), id_st,
-                           kk > 0 ? 1u : 0u);
-                mma_commit(smem_u32(&bars.dp_full));
-                // S^T of the next tile overwrites P^T_i, which dV above has read
-                // (tcgen05.mma from one thread execute in issue order)
-                if (i + 1 < n_q) {
-                    if (!(ok = mbar_wait(smem_u32(&bars.q_full[(i + 1) & 1]), ((i + 1) >> 1) & 1, wc))) break;
-                    tc_fence_after();
-                    issue_s((i + 1) & 1);
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + L::TM_DP, dV_k + koff(kk), dO_k + st * kStage + koff(kk), id_st,
+                               kk > 0 ? 1u : 0u);
+                    mma_commit(smem_u32(&bars.dp_full));
+                    // S^T_{i+1} overwrites P^T_i: wait until dV_i has read it
+                    if (i + 1 < n_q) {
+                        if (!(ok = mbar_wait(smem_u32(&bars.dv_done), i & 1, wc))) break;
+                        if (!(ok = mbar_wait(smem_u32(&bars.q_full[(i + 1) & 1]), ((i + 1) >> 1) & 1, wc))) break;
+                        issue_s((i + 1) & 1);
+                    }
                 }
-                // dK += dS^T Q ; dQ = dS K
-                if (!(ok = mbar_wait(smem_u32(&bars.ds_ready), i & 1, wc))) break;
-                tc_fence_after();
+                mma_commit(smem_u32(&bars.drain));
+                drain_wait(smem_u32(&bars.drain), 0, p.timeout_ns);
+            } else {
+                // dV_i += P^T dO, dK_i += dS^T Q, dQ_i = dS K, per query tile
+                for (int i = 0; i < n_q && ok; ++i) {
+                    const int st = i & 1;
+                    if (!(ok = mbar_wait(smem_u32(&bars.p_ready), i & 1, wc))) break;
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)
-                    mma_ss(tmem + L::TM_DK, dS_k + koff(kk), dQ_mn + st * kStage + kk * kMnStep, id_dk,
-                           (i > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        mma_ts(tmem + L::TM_DV, tmem + L::TM_S + (kk < 4 ? kk * 8 : 96 + (kk - 4) * 8),
+                               dO_mn + st * kStage + kk * kMnStep, id_dv, (i > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(smem_u32(&bars.dv_done));
+                    if (!(ok = mbar_wait(smem_u32(&bars.ds_ready), i & 1, wc))) break;
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)
-                    mma_ss(tmem + L::TM_DP, dS_mn + kk * kMnStep, dK_mn + kk * kMnStep, id_dq, kk > 0 ? 1u : 0u);
-                mma_commit(smem_u32(&bars.dq_full));
-                mma_commit(smem_u32(&bars.ds_free));
-                mma_commit(smem_u32(&bars.q_empty[st]));
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        mma_ss(tmem + L::TM_DK, dS_k + koff(kk), dQ_mn + st * kStage + kk * kMnStep, id_dk,
+                               (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        mma_ss(tmem + L::TM_DP, dS_mn + kk * kMnStep, dK_mn + kk * kMnStep, id_dq,
+                               kk > 0 ? 1u : 0u);
+                    mma_commit(smem_u32(&bars.dq_full));
+                    mma_commit(smem_u32(&bars.ds_free));
+                    mma_commit(smem_u32(&bars.q_empty[st]));
+                }
+                mma_commit(smem_u32(&bars.final_mma));
+                mma_commit(smem_u32(&bars.drain2));
+                drain_wait(smem_u32(&bars.drain2), 0, p.timeout_ns);
             }
-            mma_commit(smem_u32(&bars.final_mma));
-            mma_commit(smem_u32(&bars.drain));
-            drain_wait(smem_u32(&bars.drain), 0, p.timeout_ns);
         }
     } else if (warp < kMathWarps) {
         // ---------------------------------------------------------- P / dS math
