@@ -296,13 +296,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                     for (int kk = 0; kk < kTile / 16; ++kk)
                         mma_ss(tmem + L::TM_DK, dS_k + koff(kk), dQ_mn + st * kStage + kk * kMnStep, id_dk,
                                (i > 0 || kk > 0) ? 1u : 0u);
+                    // dK_i is the last reader of Q_i and dO_i: release the stage now,
+                    // half a tile before dQ_i completes, so the next load starts earlier
+                    mma_commit(smem_u32(&bars.q_empty[st]));
 #pragma unroll
                     for (int kk = 0; kk < kTile / 16; ++kk)
                         mma_ss(tmem + L::TM_DP, dS_mn + kk * kMnStep, dK_mn + kk * kMnStep, id_dq,
                                kk > 0 ? 1u : 0u);
                     mma_commit(smem_u32(&bars.dq_full));
                     mma_commit(smem_u32(&bars.ds_free));
-                    mma_commit(smem_u32(&bars.q_empty[st]));
                 }
                 mma_commit(smem_u32(&bars.final_mma));
                 mma_commit(smem_u32(&bars.drain2));
