@@ -13,7 +13,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libctxattn.so")
-SOURCES = ["attn_fwd.cu", "attn_bwd.cu", "ctx_api.cu"]
+SOURCES = ["attn_fwd.cu", "attn_bwd.cu", "attn_d256.cu", "ctx_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 

@@ -40,6 +40,7 @@
 // scores the other still has to read.
 #include "internal.h"
 #include "ptx.cuh"
+#include "walk.cuh"
 
 namespace ctxattn {
 namespace {
@@ -97,13 +98,6 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                  : "memory");
 }
 
-// Iteration order over the query tiles one CTA visits: for every query head
-// of the group, the ring iterations i = 0..P-1 (query chunk (c + i) mod P),
-// and the 128-row tiles of that chunk.
-struct QTileIter {
-    int h, t, it, r;
-};
-
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
     using L = BwdLayout<D>;
@@ -116,17 +110,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     const int warp = warp_id(), lane = lane_id();
     const int kt = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const ChunkTable& ct = p.ct;
-    const int P = ct.P;
     const int c = chunk_of_tile(ct, kt);
     const int kv_start = ct.off[c] + (kt - ct.tile_off[c]) * kTile;
     const int kv_len = min(kTile, ct.off[c + 1] - kv_start);
     const int G = p.group;
-    int n_q = G * ct.ntiles;  // query tiles this CTA visits (all heads of the group)
-    if (p.causal) {  // chunks after c, and the tiles of chunk c from this KV tile's row on
-        int per = ct.tile_off[c + 1] - ct.tile_off[c] - ((kv_start - ct.off[c]) >> 7);
-        for (int r2 = c + 1; r2 < P; ++r2) per += ct.tile_off[r2 + 1] - ct.tile_off[r2];
-        n_q = G * per;
-    }
+    const QWalk qw{&ct, c, p.causal, kv_start, hk * G + G};
+    const int n_q = qw.count(G);  // query tiles this CTA visits (all heads of the group)
     const WaitCtx wc{&bars.abort_flag, p.status, p.timeout_ns};
 
     if (sbase & 1023u) {  // the swizzled tiles need 1024-byte alignment
@@ -162,39 +151,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     tc_fence_after();
     const uint32_t tmem = bars.tmem_slot;
 
-    // query-tile walk: ring order from chunk c; with causal masking, tiles
-    // whose last row precedes this KV tile's first row are skipped (whole
-    // chunks before c, and the head of chunk c)
-    auto q_first_row = [&](const QTileIter& q) { return ct.off[q.r] + (q.t - ct.tile_off[q.r]) * kTile; };
-    auto visible = [&](const QTileIter& q) -> bool {
-        if (!p.causal || q.r > c) return true;
-        if (q.r < c) return false;
-        const int qs = q_first_row(q);
-        return qs + min(kTile, ct.off[q.r + 1] - qs) - 1 >= kv_start;
-    };
-    auto adv = [&](QTileIter& q) {
-        if (p.causal && q.r < c) q.t = ct.tile_off[q.r + 1] - 1;  // the whole chunk is masked
-        ++q.t;
-        if (q.t == ct.tile_off[q.r + 1]) {
-            ++q.it;
-            if (q.it == P) {
-                q.it = 0;
-                ++q.h;
-            }
-            q.r = (c + q.it) % P;
-            q.t = ct.tile_off[q.r];
-        }
-    };
-    auto next = [&](QTileIter& q) {
-        do adv(q);
-        while (q.h < hk * G + G && !visible(q));
-    };
-    QTileIter q0;
-    q0.h = hk * G;
-    q0.it = 0;
-    q0.r = c;
-    q0.t = ct.tile_off[c];
-    while (!visible(q0)) adv(q0);
+    // query-tile walk: ring order from chunk c (causal: tiles entirely
+    // above the diagonal are skipped)
+    const QTileIter q0 = qw.first(hk * G);
+    auto next = [&](QTileIter& q) { qw.next(q); };
+    auto q_first_row = [&](const QTileIter& q) { return qw.first_row(q); };
 
     if (warp == kProducerWarp) {
         // ---------------------------------------------------------- producer
@@ -507,6 +468,7 @@ int launch_bwd_d(const BwdParams& p, cudaStream_t s) {
 int launch_attn_bwd(const BwdParams& p, int D, cudaStream_t s) {
     if (D == 64) return launch_bwd_d<64>(p, s);
     if (D == 128) return launch_bwd_d<128>(p, s);
+    if (D == 256) return launch_attn_bwd256(p, s);
     return 2;
 }
 

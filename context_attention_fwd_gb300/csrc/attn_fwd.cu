@@ -33,6 +33,7 @@
 // O_x += P_x V:  A = P (TMEM), B = V (smem, MN-major: V rows are the K index).
 #include "internal.h"
 #include "ptx.cuh"
+#include "walk.cuh"
 
 namespace ctxattn {
 namespace {
@@ -86,45 +87,6 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity))
         if (globaltimer_ns() - t0 > limit_ns) break;
-}
-
-// The KV tiles the query tiles of chunk r visit.  Ring order: iteration it
-// meets chunk (r - it) mod P; all-gather order: chunk it.  With causal
-// masking, tiles whose first key lies after the CTA's last query row are
-// skipped (whole chunks after r, and the tail of chunk r).
-struct KvWalk {
-    int it, c, t, t0, t1;
-};
-struct WalkCfg {
-    int r, P, causal, allgather, q_last;
-};
-__device__ __forceinline__ void kv_set_chunk(const ChunkTable& ct, const WalkCfg& g, KvWalk& w) {
-    w.c = g.allgather ? w.it : (g.r - w.it + g.P) % g.P;
-    w.t0 = w.t = ct.tile_off[w.c];
-    w.t1 = ct.tile_off[w.c + 1];
-}
-__device__ __forceinline__ bool kv_visible(const ChunkTable& ct, const WalkCfg& g, const KvWalk& w) {
-    if (!g.causal || w.c < g.r) return true;
-    if (w.c > g.r) return false;
-    return ct.off[w.c] + (w.t - w.t0) * kTile <= g.q_last;
-}
-__device__ __forceinline__ void kv_adv(const ChunkTable& ct, const WalkCfg& g, KvWalk& w) {
-    if (g.causal && w.c > g.r) w.t = w.t1 - 1;  // the whole chunk is masked
-    if (++w.t == w.t1 && ++w.it < g.P) kv_set_chunk(ct, g, w);
-}
-__device__ __forceinline__ void kv_first(const ChunkTable& ct, const WalkCfg& g, KvWalk& w) {
-    w.it = 0;
-    kv_set_chunk(ct, g, w);
-    while (w.it < g.P && !kv_visible(ct, g, w)) kv_adv(ct, g, w);
-}
-__device__ __forceinline__ void kv_next(const ChunkTable& ct, const WalkCfg& g, KvWalk& w) {
-    do kv_adv(ct, g, w);
-    while (w.it < g.P && !kv_visible(ct, g, w));
-}
-// Number of tiles the walk visits.
-__device__ __forceinline__ int kv_count(const ChunkTable& ct, const WalkCfg& g) {
-    if (!g.causal) return ct.ntiles;
-    return ct.tile_off[g.r] + ((g.q_last - ct.off[g.r]) >> 7) + 1;
 }
 
 template <int D, bool kPartials>
@@ -452,6 +414,7 @@ int launch_fwd_d(const FwdParams& p, cudaStream_t s) {
 int launch_attn_fwd(const FwdParams& p, int D, cudaStream_t s) {
     if (D == 64) return launch_fwd_d<64>(p, s);
     if (D == 128) return launch_fwd_d<128>(p, s);
+    if (D == 256) return launch_attn_fwd256(p, s);
     return 2;
 }
 

@@ -368,7 +368,7 @@ int ctx_attn_fwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
     if (B > INT32_MAX || S > INT32_MAX || Hq > 65535 || Hkv > 65535 || B > 65535)
         return CTX_ERR_INVALID_ARG;
     if (!sizes_ok((int)B, (int)S, (int)Hq, (int)Hkv, (int)D)) return CTX_ERR_INVALID_ARG;
-    if (D != 64 && D != 128) return CTX_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128 && D != 256) return CTX_ERR_UNSUPPORTED;
     if (causal && (flags & CTX_FLAG_MATERIALIZE_PARTIALS)) return CTX_ERR_UNSUPPORTED;
     Dense dq_, dk_, dv_, do_;
     int rc;
@@ -391,7 +391,8 @@ int ctx_attn_fwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
     }
     if (!make_tmap_bshd(&p.tq, dq_.data, B, S, Hq, D, dq_.sb, dq_.ss, dq_.sh, 64, kTile) ||
         !make_tmap_bshd(&p.tk, dk_.data, B, S, Hkv, D, dk_.sb, dk_.ss, dk_.sh, 64, kTile) ||
-        !make_tmap_bshd(&p.tv, dv_.data, B, S, Hkv, D, dv_.sb, dv_.ss, dv_.sh, 64, kTile))
+        // D = 256 streams V in 64-row halves (each half is one PV k-range)
+        !make_tmap_bshd(&p.tv, dv_.data, B, S, Hkv, D, dv_.sb, dv_.ss, dv_.sh, 64, D == 256 ? 64 : kTile))
         return CTX_ERR_CUDA;
     p.B = (int)B; p.S = (int)S; p.Hq = (int)Hq; p.Hkv = (int)Hkv;
     p.group = (int)(Hq / Hkv);
@@ -432,7 +433,8 @@ int ctx_attn_bwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
     if (B > INT32_MAX || S > INT32_MAX || Hq > 65535 || Hkv > 65535 || B > 65535)
         return CTX_ERR_INVALID_ARG;
     if (!sizes_ok((int)B, (int)S, (int)Hq, (int)Hkv, (int)D)) return CTX_ERR_INVALID_ARG;
-    if (D != 64 && D != 128) return CTX_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128 && D != 256) return CTX_ERR_UNSUPPORTED;
+    if (D == 256 && B > 32767) return CTX_ERR_INVALID_ARG;  // grid z = 2 B (column halves)
     Dense tq, tk, tv, to, tdo, tdq, tdk, tdv;
     int rc;
     if ((rc = resolve(q, B, S, Hq, D, layout, &tq))) return rc;

@@ -70,5 +70,8 @@ struct BwdParams {
 
 int launch_attn_fwd(const FwdParams& p, int D, cudaStream_t s);
 int launch_attn_bwd(const BwdParams& p, int D, cudaStream_t s);
+// head dimension 256 (attn_d256.cu); the forward's V map uses 64-row boxes
+int launch_attn_fwd256(const FwdParams& p, cudaStream_t s);
+int launch_attn_bwd256(const BwdParams& p, cudaStream_t s);
 
 }  // namespace ctxattn

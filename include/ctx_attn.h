@@ -24,7 +24,10 @@
  *  - Arguments are validated before anything is launched; an invalid call
  *    returns an error code and writes nothing (never a silent wrong result).
  *  - Element type: bf16 for q, k, v, out, dout, dq, dk, dv; fp32 for lse.
- *  - Head dimension D is 64 or 128 (others: CTX_ERR_UNSUPPORTED).
+ *  - Head dimension D is 64, 128 or 256 (others: CTX_ERR_UNSUPPORTED).  D = 256
+ *    is the Hugging Face causal model of the DeepSpeed Ulysses pull request
+ *    ("24 attention heads, 4 key/value heads, head dimension 256"); its
+ *    backward additionally needs B <= 32767.
  *  - Chunks: chunk_offsets == NULL means numpy-array_split chunking (the first
  *    S mod P chunks are one row longer); otherwise a host array of P+1
  *    strictly increasing offsets from 0 to S.  Empty chunks are rejected.

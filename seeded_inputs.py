@@ -34,6 +34,10 @@ MHA_B2_S512_P2 = AttnShape(B=2, S=512, Hq=8, Hkv=8, D=64, P=2, layout="bshd")
 SEQFIRST_S1001_P4 = AttnShape(B=1, S=1001, Hq=16, Hkv=16, D=64, P=4, layout="sbhd")
 FLUX_GQA_S4608_P4 = AttnShape(B=1, S=4608, Hq=24, Hkv=8, D=128, P=4, layout="bshd")
 VIDEO_S32760_P8 = AttnShape(B=1, S=32760, Hq=24, Hkv=24, D=128, P=8, layout="bshd")
+# causal language model of the DeepSpeed Ulysses pull request's end-to-end
+# check: 24 query heads, 4 key/value heads, head dimension 256, 1024 tokens,
+# sequence parallelism 2 (and 8)
+GQA_D256_S1024 = AttnShape(B=1, S=1024, Hq=24, Hkv=4, D=256, P=2, layout="bshd")
 # ring 4 x ulysses 2 hybrid: exchange of [1,65536,32,128] (+ k, v with 8 heads),
 # then GQA 32/8 attention over 4 ring chunks on the exchanged tensors.
 HYBRID_S65536 = AttnShape(B=1, S=65536, Hq=32, Hkv=8, D=128, P=4, layout="bshd")
