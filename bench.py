@@ -31,7 +31,7 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from seeded_inputs import VIDEO_S32760_P8, AttnShape, attn_inputs, exchange_input  # noqa: E402
+from seeded_inputs import GQA_D256_S1024, VIDEO_S32760_P8, AttnShape, attn_inputs, exchange_input  # noqa: E402
 
 METRIC = "fwd+bwd attention TFLOP/s at 1 GB300 (ring P chunks), % of dense bf16 peak"
 UNIT = "TFLOP/s"
@@ -41,8 +41,8 @@ L2_NOTE = "inputs larger than L2 (q/k/v/dout 805 MB vs 126.5 MB L2); no flush"
 
 # dram traffic per launch of the backward kernel from one ncu capture (see
 # profiles/); valid only while the kernel source is the one it was taken on.
-NCU_BWD = {"bytes_per_launch": 1307783168 + 873230848,  # dram read + write, S=32760 H=24 D=128 P=8
-           "source_sha256": "6e32cc0a3de9943c1768b7c85018e4fd0699242861f55999b529e32b49c98a03"}
+NCU_BWD = {"bytes_per_launch": 1335383040 + 895592448,  # dram read + write, S=32760 H=24 D=128 P=8
+           "source_sha256": "4f0bf6a0924f3ed8193af22c6fb6737b2ede073cb32d68f88aa6e553c2e5812b"}
 
 
 def flops_fwd(sh: AttnShape) -> float:
@@ -196,6 +196,58 @@ def measure_exchange(ctx, dev, stream, barrier, peaks):
             "bytes": xbytes}
 
 
+def measure_d256(ctx, dev, stream, barrier, peaks):
+    """Head dimension 256: the 24/4-head causal language model (1024 tokens,
+    P=2; inputs 14 MB, resident in L2) and a long-context case of the same
+    heads (16384 tokens, P=8).  Causal flop count: the S (S + 1) / 2 visible
+    pairs, 4 D flop each forward and 10 D backward, per query head."""
+    res = []
+    for name, sh, reps in (("24/4-head D=256 causal LM, S=1024, P=2", GQA_D256_S1024, 50),
+                           ("same heads, long context S=16384, P=8",
+                            AttnShape(B=1, S=16384, Hq=24, Hkv=4, D=256, P=8), 5)):
+        q, k, v, do = (t.to(dev) for t in attn_inputs(sh))
+        out, lse = ctx.attn_fwd(q, k, v, sh.P, causal=True)
+        ws = torch.empty(ctx.workspace_size(sh.B, sh.S, sh.Hq, sh.Hkv, sh.D, sh.P), dtype=torch.uint8,
+                         device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def step():
+            ctx.attn_fwd(q, k, v, sh.P, causal=True, out=out, lse=lse)
+            ctx.attn_bwd(q, k, v, out, lse, do, sh.P, causal=True, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+        for _ in range(3):
+            step()
+        barrier()
+        ctx.profile_enable(True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            step()
+        e1.record(stream)
+        barrier()
+        ctx.profile_enable(False)
+        if ctx.device_status() != 0:
+            raise RuntimeError("device-side wait timed out (D=256)")
+        ms = e0.elapsed_time(e1) / reps
+        pairs = sh.B * sh.Hq * sh.S * (sh.S + 1) / 2.0
+        fl_f, fl_b = 4.0 * pairs * sh.D, 10.0 * pairs * sh.D
+        f_ms, f_n = ctx.profile_read("fwd")
+        b_ms, b_n = ctx.profile_read("bwd")
+        f_avg, b_avg = f_ms / max(f_n, 1), b_ms / max(b_n, 1)
+        res.append({"workload": name, "B": sh.B, "S": sh.S, "Hq": sh.Hq, "Hkv": sh.Hkv, "D": sh.D,
+                    "P": sh.P, "causal": True, "ms_per_step": ms,
+                    "value": (fl_f + fl_b) / (ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                    "fwd_kernel": {"kernel": "attn_fwd256_kernel", "avg_ms": f_avg,
+                                   "achieved": fl_f / (f_avg / 1e3) / 1e12,
+                                   "frac": fl_f / (f_avg / 1e3) / 1e12 / peaks["bf16"]},
+                    "bwd_kernel": {"kernel": "attn_bwd256_kernel", "avg_ms": b_avg,
+                                   "achieved": fl_b / (b_avg / 1e3) / 1e12,
+                                   "frac": fl_b / (b_avg / 1e3) / 1e12 / peaks["bf16"]},
+                    "peak": peaks["bf16"], "peak_kind": f"bf16 dense, burst ({peaks['source']})"})
+        del q, k, v, do, out, lse, ws, dq, dk, dv
+    return res
+
+
 def measure_e2e(ctx, dev, sh, host_inputs, ws, steps, barrier, world):
     """End to end through the public API: every step copies that step's
     inputs (q, k, v, dout) from pinned host memory to the GPU, runs the
@@ -280,6 +332,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-exchange", action="store_true")
+    ap.add_argument("--no-d256", action="store_true")
     ap.add_argument("--shape", default=None,
                     help="S,Hq,Hkv,D,P: a smaller case of the same kernels (profiler captures)")
     args = ap.parse_args()
@@ -373,6 +426,11 @@ def main():
     if not args.no_exchange:
         exchange = measure_exchange(ctx, dev, stream, barrier, peaks)
 
+    # ------------------------------------------------ head dimension 256 (GQA 24/4, causal)
+    d256 = None
+    if not args.no_d256:
+        d256 = measure_d256(ctx, dev, stream, barrier, peaks)
+
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
@@ -391,14 +449,15 @@ def main():
                          "peak": peak, "unit": "TFLOP/s", "frac": fwd_tf / peak,
                          "launches": fwd_n, "avg_ms": fwd_avg},
         "exchange": exchange,
+        "d256": d256,
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        val, secs = cpu_sample(8190)
+        val, secs = cpu_sample(16380)
         line["cpu_baseline"] = {
             "value": val, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
             "sample": ("fp64 oracle forward + analytic backward of head 0 of the workload truncated "
-                       f"to its first two ring chunks (S=8190, D=128), {secs:.1f} s")}
+                       f"to its first four ring chunks (S=16380, D=128), {secs:.1f} s")}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
