@@ -413,14 +413,17 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
     const uint32_t sK = sbase + L::OFF_K, sRing = sbase + L::OFF_RING, sDS = sbase + L::OFF_DS;
     const float* stat_base = reinterpret_cast<const float*>(smem + L::OFF_STAT);
     const int warp = warp_id(), lane = lane_id();
-    const int kt = blockIdx.x, hk = blockIdx.y, b = blockIdx.z >> 1, hh = blockIdx.z & 1;
+    // z = 2 (b * hsplit + split) + column half
+    const int kt = blockIdx.x, hk = blockIdx.y, hh = blockIdx.z & 1;
+    const int b = (blockIdx.z >> 1) / p.hsplit, split = (blockIdx.z >> 1) % p.hsplit;
     const ChunkTable& ct = p.ct;
     const int c = chunk_of_tile(ct, kt);
     const int kv_start = ct.off[c] + (kt - ct.tile_off[c]) * kTile;
     const int kv_len = min(kTile, ct.off[c + 1] - kv_start);
-    const int G = p.group;
-    const QWalk qw{&ct, c, p.causal, kv_start, hk * G + G};
-    const int n_q = qw.count(G);
+    const int Gs = p.group / p.hsplit;       // query heads of this CTA
+    const int h0 = hk * p.group + split * Gs;
+    const QWalk qw{&ct, c, p.causal, kv_start, h0 + Gs};
+    const int n_q = qw.count(Gs);
     const WaitCtx wc{&bars.abort_flag, p.status, p.timeout_ns};
 
     if (sbase & 1023u) {
@@ -455,7 +458,11 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars.tmem_slot;
-    const QTileIter q0 = qw.first(hk * G);
+    const QTileIter q0 = qw.first(h0);
+    // fp32 partial rows of this CTA's (split, b, hk) when the group is split
+    float* const part_row = p.dkv_part
+        ? p.dkv_part + ((((size_t)(split * p.B + b) * p.Hkv + hk) * p.S + kv_start) * 2) * kD + hh * 128
+        : nullptr;
     auto slot_of = [](int n) { return n % L::SLOTS; };
     auto phase_of = [](int n) { return (n / L::SLOTS) & 1; };
     auto full_bar = [&](int n) { return smem_u32(&bars.full[n % L::SLOTS]); };
@@ -685,7 +692,13 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
                 tmem_ld32(taddr + L::TM_DV + half * 64 + cc * 32, o);
                 tmem_ld_wait();
                 reg_fence32(o);
-                if (row_valid) {
+                if (row_valid && part_row) {  // fp32 partial, summed by dkv_reduce_kernel
+                    float4* d4 = reinterpret_cast<float4*>(part_row + ((size_t)row * 2 + 1) * kD + half * 64 + cc * 32);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        d4[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                            __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
+                } else if (row_valid) {
                     uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
@@ -741,7 +754,13 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
                 tmem_ld32(taddr + L::TM_DK + cc * 32, o);
                 tmem_ld_wait();
                 reg_fence32(o);
-                if (row_valid) {
+                if (row_valid && part_row) {  // unscaled fp32 partial
+                    float4* d4 = reinterpret_cast<float4*>(part_row + (size_t)row * 2 * kD + cc * 32);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        d4[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                            __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
+                } else if (row_valid) {
                     uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
@@ -777,7 +796,7 @@ int launch_attn_bwd256(const BwdParams& p, cudaStream_t s) {
     if (cudaFuncSetAttribute(attn_bwd256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, B256::SMEM) !=
         cudaSuccess)
         return 4;
-    dim3 grid(p.ct.ntiles, p.Hkv, p.B * 2);  // z = 2 b + column half
+    dim3 grid(p.ct.ntiles, p.Hkv, p.B * 2 * p.hsplit);  // z = 2 (b * hsplit + split) + column half
     attn_bwd256_kernel<<<grid, kB256Threads, B256::SMEM, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }

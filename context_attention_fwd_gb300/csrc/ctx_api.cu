@@ -220,6 +220,37 @@ __global__ void dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* 
     *reinterpret_cast<uint4*>(dq + b * sb + (int64_t)s * ss + h * sh + k8 * 8) = v;
 }
 
+// Sum of the head-split partial dK / dV of the D = 256 backward:
+// part [hs][B][Hkv][S][2][D] fp32 (dK unscaled, dV) -> dk = scale * sum,
+// dv = sum, bf16 rows of the caller's layout.  One thread per 8 columns.
+__global__ void dkv_reduce_kernel(const float* __restrict__ part, int hs, int B, int Hkv, int S, int D,
+                                  __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
+                                  int64_t sb, int64_t ss, int64_t sh, float scale) {
+    const int g8 = D / 8;
+    const int64_t n = (int64_t)B * Hkv * S * 2;  // (b, hk, s, which) rows
+    const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (gt >= n * g8) return;
+    const int64_t r = gt / g8;
+    const int k8 = (int)(gt - r * g8);
+    const int which = (int)(r & 1);
+    const int64_t bhs = r >> 1;
+    const int s = (int)(bhs % S);
+    const int64_t bh = bhs / S;
+    const int hk = (int)(bh % Hkv), b = (int)(bh / Hkv);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int i = 0; i < hs; ++i) {
+        const float4* src = reinterpret_cast<const float4*>(part + ((int64_t)i * n + r) * D + k8 * 8);
+        const float4 lo = src[0], hi = src[1];
+        acc[0] += lo.x; acc[1] += lo.y; acc[2] += lo.z; acc[3] += lo.w;
+        acc[4] += hi.x; acc[5] += hi.y; acc[6] += hi.z; acc[7] += hi.w;
+    }
+    const float f = which == 0 ? scale : 1.f;
+    uint4 v = make_uint4(pack_bf16x2(acc[0] * f, acc[1] * f), pack_bf16x2(acc[2] * f, acc[3] * f),
+                         pack_bf16x2(acc[4] * f, acc[5] * f), pack_bf16x2(acc[6] * f, acc[7] * f));
+    __nv_bfloat16* dst = (which == 0 ? dk : dv) + b * sb + (int64_t)s * ss + hk * sh + k8 * 8;
+    *reinterpret_cast<uint4*>(dst) = v;
+}
+
 // LSE merge of materialised partials: L = log sum_i exp(LSE_i),
 // O = sum_i exp(LSE_i - L) O_i.  part_o [P][B][H][S][D], part_lse [P][B][H][S].
 // One thread per 4 columns of a row.
@@ -307,9 +338,24 @@ size_t fwd_ws_bytes(int B, int S, int Hq, int D, int P, int flags) {
     return align256(rows * D * 4) + align256(rows * 4);
 }
 
-size_t bwd_ws_bytes(int B, int S, int Hq, int D, int P) {
+// D = 256 backward: CTAs per (KV tile, column half) that share the query
+// heads of one GQA group, chosen so that the grid fills about one wave of a
+// 148..152-SM GPU when the sequence is short.  Non-increasing in ntiles.
+int bwd_hsplit(int64_t ntiles, int B, int Hq, int Hkv, int D) {
+    if (D != 256) return 1;
+    const int G = Hq / Hkv;
+    const int64_t base = ntiles * Hkv * 2 * B;
+    for (int d = 1; d < G; ++d)
+        if (G % d == 0 && base * d >= 148) return d;
+    return G;
+}
+
+size_t bwd_ws_bytes(int B, int S, int Hq, int Hkv, int D, int P) {
     const size_t slots = (size_t)B * Hq * ntiles_upper(S, P) * kTile;
-    return align256(slots * 4) * 2 + align256(slots * D * 4);
+    // every chunking has at least ceil(S / 128) tiles: the largest split
+    const int hs = bwd_hsplit((S + kTile - 1) / kTile, B, Hq, Hkv, D);
+    const size_t part = hs > 1 ? align256((size_t)hs * B * Hkv * S * 2 * D * 4) : 0;
+    return align256(slots * 4) * 2 + align256(slots * D * 4) + part;
 }
 
 bool sizes_ok(int B, int S, int Hq, int Hkv, int D) {
@@ -347,7 +393,7 @@ int ctx_chunk_offsets(int S, int P, int* off) {
 size_t ctx_attn_workspace_size(int B, int S, int Hq, int Hkv, int D, int P, int flags) {
     if (!sizes_ok(B, S, Hq, Hkv, D) || P < 1 || P > S || P > kMaxChunks) return 0;
     const size_t f = fwd_ws_bytes(B, S, Hq, D, P, flags);
-    const size_t b = bwd_ws_bytes(B, S, Hq, D, P);
+    const size_t b = bwd_ws_bytes(B, S, Hq, Hkv, D, P);
     return f > b ? f : b;
 }
 
@@ -450,7 +496,7 @@ int ctx_attn_bwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
     BwdParams p;
     memset(&p, 0, sizeof(p));
     if ((rc = build_chunks((int)S, P, chunk_offsets, &p.ct))) return rc;
-    const size_t need = bwd_ws_bytes((int)B, (int)S, (int)Hq, (int)D, P);
+    const size_t need = bwd_ws_bytes((int)B, (int)S, (int)Hq, (int)Hkv, (int)D, P);
     if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
         return CTX_ERR_WORKSPACE;
     const size_t slots = (size_t)B * Hq * p.ct.ntiles * kTile;
@@ -458,6 +504,10 @@ int ctx_attn_bwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
     float* lse2_t = reinterpret_cast<float*>(ws);
     float* delta_t = reinterpret_cast<float*>(ws + align256(slots * 4));
     float* dq_acc = reinterpret_cast<float*>(ws + 2 * align256(slots * 4));
+    p.hsplit = bwd_hsplit(p.ct.ntiles, (int)B, (int)Hq, (int)Hkv, (int)D);
+    if ((int64_t)B * 2 * p.hsplit > 65535) p.hsplit = 1;  // grid z limit (B <= 32767 checked above)
+    p.dkv_part = p.hsplit > 1 ? reinterpret_cast<float*>(ws + 2 * align256(slots * 4) + align256(slots * D * 4))
+                              : nullptr;
     if (!make_tmap_bshd(&p.tq, tq.data, B, S, Hq, D, tq.sb, tq.ss, tq.sh, 64, kTile) ||
         !make_tmap_bshd(&p.tk, tk.data, B, S, Hkv, D, tk.sb, tk.ss, tk.sh, 64, kTile) ||
         !make_tmap_bshd(&p.tv, tv.data, B, S, Hkv, D, tv.sb, tv.ss, tv.sh, 64, kTile) ||
@@ -492,6 +542,14 @@ int ctx_attn_bwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
     rc = launch_attn_bwd(p, (int)D, s);
     prof_record(1, 1, s);
     if (rc) return rc;
+    if (p.dkv_part) {
+        const int64_t threads = B * Hkv * S * 2 * (D / 8);
+        const int blk = 256;
+        dkv_reduce_kernel<<<(unsigned)((threads + blk - 1) / blk), blk, 0, s>>>(
+            p.dkv_part, p.hsplit, (int)B, (int)Hkv, (int)S, (int)D, p.dk, p.dv, p.k_sb, p.k_ss, p.k_sh,
+            p.scale);
+        if ((rc = launch_status())) return rc;
+    }
     {
         const int64_t threads = (int64_t)slots * (D / 8);
         const int blk = 256;

@@ -64,6 +64,12 @@ struct BwdParams {
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
     int64_t k_sb, k_ss, k_sh;  // strides of dk/dv
+    // D = 256 only: the query heads of a GQA group are split over hsplit
+    // CTAs per (KV tile, column half); with hsplit > 1 each writes fp32
+    // partial dK (unscaled) / dV to dkv_part [hsplit][B][Hkv][S][2][D] and
+    // dkv_reduce_kernel sums them
+    int hsplit;
+    float* dkv_part;
     int* status;
     uint64_t timeout_ns;
 };

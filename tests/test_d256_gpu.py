@@ -88,3 +88,14 @@ def test_d256_equals_two_d128_halves_of_v():
         sl = slice(half * 128, (half + 1) * 128)
         assert torch.equal(oh[..., sl], out[..., sl])
         assert oh[..., (1 - half) * 128:(2 - half) * 128].abs().max().item() == 0
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,P", [(2, 1300, 8, 4, 2),   # enough KV tiles: one CTA per group
+                                          (1, 1000, 12, 2, 3),  # short: the group of 6 split 3 ways
+                                          (1, 600, 6, 1, 1)])   # a single KV head: split 6 ways
+def test_gqa_group_split(B, S, Hq, Hkv, P):
+    """The backward splits a GQA group's query heads over several CTAs when
+    the sequence is short (partial dK/dV summed afterwards) and keeps one CTA
+    per group otherwise; both give the oracle's gradients."""
+    sh = AttnShape(B=B, S=S, Hq=Hq, Hkv=Hkv, D=256, P=P)
+    check_full(*run_gpu(sh))
