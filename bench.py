@@ -127,6 +127,24 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest x over the ranks of the default process group (the
+    slowest replica's time); x itself without one."""
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item()
+
+
+def replica_throughput(flops_per_step: float, steps: int, ms: float, world: int) -> float:
+    """Whole-job TFLOP/s of `world` independent replicas, each doing `steps`
+    steps, timed by the slowest replica (ms)."""
+    return world * flops_per_step * steps / (ms / 1e3) / 1e12
+
+
 def cpu_sample(S_sample: int):
     """Times the fp64 oracle (forward + analytic backward) on head 0 of the
     workload truncated to its first S_sample rows; returns (TFLOP/s, seconds)."""
@@ -135,6 +153,9 @@ def cpu_sample(S_sample: int):
     sh = AttnShape(B=1, S=S_sample, Hq=1, Hkv=1, D=WORKLOAD.D, P=1)
     q, k, v, do = attn_inputs(sh, seed=777)
     oracle.build()
+    # every host core (torchrun pins OMP_NUM_THREADS to 1 per rank, and only
+    # rank 0 runs the oracle)
+    oracle.set_threads(os.cpu_count())
     t0 = time.perf_counter()
     oracle.attn_fwd(q, k, v)
     oracle.attn_bwd(q, k, v, do)
@@ -304,15 +325,11 @@ def measure_e2e(ctx, dev, sh, host_inputs, ws, steps, barrier, world):
     compute.wait_event(out_free[(steps - 1) % nbuf])
     e1.record(compute)
     barrier()
-    ems = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ems], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ems = t.item()
+    ems = max_over_ranks(e0.elapsed_time(e1), dev)
     flops_step = flops_fwd(sh) + flops_bwd(sh)
     h2d = sum(t.numel() * t.element_size() for t in h_in)
     d2h = sum(t.numel() * t.element_size() for t in h_out[0])
-    return {"value": world * flops_step * steps / (ems / 1e3) / 1e12, "unit": UNIT,
+    return {"value": replica_throughput(flops_step, steps, ems, world), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems / steps,
             "overlap": "copies on their own streams, inputs/outputs double-buffered",
             "gpu_launches": 4 * steps}
@@ -396,15 +413,11 @@ def main():
         ev1.record(stream)
         barrier()
     ctx.profile_enable(False)
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = t.item()
+    ms = max_over_ranks(ev0.elapsed_time(ev1), dev)
     if ctx.device_status() != 0:
         raise RuntimeError("device-side wait timed out during the timed region")
     flops_step = flops_fwd(sh) + flops_bwd(sh)
-    value = world * flops_step * args.steps / (ms / 1e3) / 1e12
+    value = replica_throughput(flops_step, args.steps, ms, world)
     bwd_ms, bwd_n = ctx.profile_read("bwd")
     fwd_ms, fwd_n = ctx.profile_read("fwd")
     bwd_avg, fwd_avg = bwd_ms / max(bwd_n, 1), fwd_ms / max(fwd_n, 1)

@@ -58,8 +58,15 @@ def _load():
                          "oracle_attn_dq_rows", "oracle_attn_dkv_rows", "oracle_ring_fwd",
                          "oracle_lse_merge", "oracle_ring_bwd", "oracle_seq_head_exchange"):
                 getattr(lib, name).restype = ctypes.c_int
+            lib.oracle_set_threads.restype = None
             _lib = lib
     return _lib
+
+
+def set_threads(n: int) -> None:
+    """OpenMP threads for the oracle's loops run from this thread (the
+    arithmetic does not depend on it)."""
+    _load().oracle_set_threads(int(n))
 
 
 def _f64(t: torch.Tensor) -> torch.Tensor:

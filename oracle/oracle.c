@@ -42,9 +42,17 @@
  * The log-sum-exp array is [B,H,S] contiguous.
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+
+/* Number of OpenMP threads of the calling thread's later parallel loops (a
+ * launcher may have pinned OMP_NUM_THREADS before the runtime started);
+ * no arithmetic depends on it. */
+void oracle_set_threads(int n) {
+    if (n > 0) omp_set_num_threads(n);
+}
 
 #define AT(p, st, b, s, h) ((p) + (long)(b) * (st)[0] + (long)(s) * (st)[1] + (long)(h) * (st)[2])
 
