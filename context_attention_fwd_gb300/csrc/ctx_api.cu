@@ -115,37 +115,59 @@ int64_t ntiles_upper(int S, int P) {  // tiles of any chunking of S into P chunk
 
 // ---------------------------------------------------------------- kernels
 
-// Ulysses exchange: one y row (u, b, s) of Hu*D elements per iteration of a
-// block-stride loop; 16-byte vectors inside the row.
+// Ulysses exchange: y rows (u, b, s) of Hu*D elements, 16-byte vectors
+// inside a row.  Each block takes kExRows rows per iteration of a
+// block-stride loop and issues all their loads before any store, so that
+// enough bytes are in flight to cover HBM latency.
+constexpr int kExRows = 4;
+
+__device__ __forceinline__ void exchange_row_index(int64_t ri, int B, int64_t Sp, int layout, int64_t& u,
+                                                   int64_t& bb, int64_t& s) {
+    u = ri / ((int64_t)B * Sp);
+    const int64_t rem = ri - u * B * Sp;
+    if (layout == 0) {  // [U][B][Sp]
+        bb = rem / Sp;
+        s = rem - bb * Sp;
+    } else {  // [U][Sp][B]
+        s = rem / B;
+        bb = rem - s * B;
+    }
+}
+
 __global__ void exchange_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ y, int B,
                                 int S, int Hu, int D, int64_t xsb, int64_t xss, int64_t xsh,
                                 int64_t Sp, int layout, int dir, int64_t nrows) {
     const int vec_per_head = D / 8;
     const int vec_per_row = Hu * vec_per_head;
-    for (int64_t ri = blockIdx.x; ri < nrows; ri += gridDim.x) {
-        int64_t u, bb, s;
-        if (layout == 0) {  // [U][B][Sp]
-            u = ri / ((int64_t)B * Sp);
-            const int64_t rem = ri - u * B * Sp;
-            bb = rem / Sp;
-            s = rem - bb * Sp;
-        } else {  // [U][Sp][B]
-            u = ri / ((int64_t)B * Sp);
-            const int64_t rem = ri - u * B * Sp;
-            s = rem / B;
-            bb = rem - s * B;
+    for (int64_t r0 = (int64_t)blockIdx.x * kExRows; r0 < nrows; r0 += (int64_t)gridDim.x * kExRows) {
+        int64_t xrow[kExRows];
+        bool real[kExRows], live[kExRows];
+#pragma unroll
+        for (int k = 0; k < kExRows; ++k) {
+            int64_t u, bb, s;
+            live[k] = r0 + k < nrows;
+            exchange_row_index(live[k] ? r0 + k : 0, B, Sp, layout, u, bb, s);
+            real[k] = live[k] && s < S;
+            xrow[k] = bb * xsb + s * xss + u * Hu * xsh;
         }
-        uint4* yrow = reinterpret_cast<uint4*>(y + ri * Hu * D);
-        const bool real = s < S;
-        const int64_t xrow = bb * xsb + s * xss + u * Hu * xsh;
         for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) {
             const int hh = v / vec_per_head, d8 = v - hh * vec_per_head;
-            const int64_t xo = xrow + hh * xsh + d8 * 8;
+            const int64_t off = hh * xsh + d8 * 8;
+            uint4 val[kExRows];
             if (dir == 0) {
-                yrow[v] = real ? *reinterpret_cast<const uint4*>(x + xo) : make_uint4(0, 0, 0, 0);
-            } else if (real) {
-                *reinterpret_cast<uint4*>(const_cast<uint16_t*>(x) + xo) =
-                    reinterpret_cast<const uint4*>(yrow)[v];
+#pragma unroll
+                for (int k = 0; k < kExRows; ++k)
+                    val[k] = real[k] ? *reinterpret_cast<const uint4*>(x + xrow[k] + off) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int k = 0; k < kExRows; ++k)
+                    if (live[k]) reinterpret_cast<uint4*>(y + (r0 + k) * Hu * D)[v] = val[k];
+            } else {
+#pragma unroll
+                for (int k = 0; k < kExRows; ++k)
+                    if (real[k]) val[k] = reinterpret_cast<const uint4*>(y + (r0 + k) * Hu * D)[v];
+#pragma unroll
+                for (int k = 0; k < kExRows; ++k)
+                    if (real[k]) *reinterpret_cast<uint4*>(const_cast<uint16_t*>(x) + xrow[k] + off) = val[k];
             }
         }
     }
@@ -623,7 +645,8 @@ int ctx_seq_head_exchange(const ctx_tensor_t* x, void* y, int ring, int ulysses,
     const int vec_per_row = Hu * (int)(D / 8);
     int blk = 32;
     while (blk < vec_per_row && blk < 512) blk *= 2;
-    const int64_t grid = nrows < (int64_t)num_sms() * 16 ? nrows : (int64_t)num_sms() * 16;
+    const int64_t nblk = (nrows + kExRows - 1) / kExRows;
+    const int64_t grid = nblk < (int64_t)num_sms() * 16 ? nblk : (int64_t)num_sms() * 16;
     exchange_kernel<<<(unsigned)grid, blk, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t*>(tx.data), static_cast<uint16_t*>(y), (int)B, (int)S, Hu, (int)D,
         tx.sb, tx.ss, tx.sh, Sp, layout == CTX_LAYOUT_BSHD ? 0 : 1, dir, nrows);

@@ -103,6 +103,12 @@ def test_invalid_arguments_fail_before_launch(lib):
         ctypes.byref(kw.get("out", out)), kw.get("lse", lse), None, 0, kw.get("flags", 0), None)
     assert call(P=0) == 1                               # P < 1
     assert call(P=65) == 1                              # P > S
+    big_q, big_kv, big_o = _t(fake, 1, 1000, 4, 64), _t(fake, 1, 1000, 2, 64), _t(fake, 1, 1000, 4, 64)
+    assert call(q=big_q, k=big_kv, v=big_kv, out=big_o, P=65) == 1  # more chunks than the table holds
+    for empty in ((0, 64, 4, 64), (1, 0, 4, 64), (1, 64, 0, 64), (1, 64, 4, 0)):  # empty inputs
+        B_, S_, H_, D_ = empty
+        e = _t(fake, B_, S_, H_, D_)
+        assert call(q=e, k=e, v=e, out=e) == 1, empty
     assert call(k=_t(fake, 1, 64, 3, 64), v=_t(fake, 1, 64, 3, 64)) == 1  # Hq % Hkv
     assert call(layout=7) == 1
     assert call(lse=None) == 1

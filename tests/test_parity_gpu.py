@@ -81,6 +81,14 @@ def test_every_p_gqa(P, D):
     check_full(*run_gpu(sh))
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_max_chunks_p64(causal):
+    """The largest chunk table: 64 ring chunks of 15-16 rows (every chunk a
+    single partial tile)."""
+    sh = AttnShape(B=1, S=1000, Hq=4, Hkv=2, D=64, P=64)
+    check_full(*run_gpu(sh, causal=causal), causal=causal)
+
+
 def test_custom_chunk_offsets():
     sh = AttnShape(B=2, S=700, Hq=2, Hkv=1, D=128, P=4)
     check_full(*run_gpu(sh, offsets=[0, 1, 300, 429, 700]))
