@@ -424,7 +424,11 @@ def main():
     bwd_tf = flops_bwd(sh) / (bwd_avg / 1e3) / 1e12
     fwd_tf = flops_fwd(sh) / (fwd_avg / 1e3) / 1e12
     bwd_src = os.path.join(ROOT, "context_attention_fwd_gb300", "csrc", "attn_bwd.cu")
-    traffic = NCU_BWD["bytes_per_launch"] if NCU_BWD["source_sha256"] == source_sha(bwd_src) else None
+    # the ncu bytes were taken on the default workload, with this source
+    traffic = (NCU_BWD["bytes_per_launch"]
+               if not args.shape and NCU_BWD["source_sha256"] == source_sha(bwd_src) else None)
+    kname = "attn_fwd256_kernel" if sh.D == 256 else f"attn_fwd_kernel<{sh.D}>"
+    bname = "attn_bwd256_kernel" if sh.D == 256 else f"attn_bwd_kernel<{sh.D}>"
     peak = peaks["bf16_sustained"]
     clocks = clk.summary()
 
@@ -454,11 +458,11 @@ def main():
                         "peaks_source": peaks["source"]},
         "clocks": clocks,
         "gpu_launches": 4 * args.steps,
-        "roofline": {"kernel": "attn_bwd_kernel<128>", "bound": "tensor", "achieved": bwd_tf,
+        "roofline": {"kernel": bname, "bound": "tensor", "achieved": bwd_tf,
                      "peak": peak, "unit": "TFLOP/s", "frac": bwd_tf / peak, "traffic": traffic,
                      "peak_kind": f"bf16 dense, sustained ({peaks['source']})",
                      "launches": bwd_n, "avg_ms": bwd_avg},
-        "roofline_fwd": {"kernel": "attn_fwd_kernel<128>", "bound": "tensor", "achieved": fwd_tf,
+        "roofline_fwd": {"kernel": kname, "bound": "tensor", "achieved": fwd_tf,
                          "peak": peak, "unit": "TFLOP/s", "frac": fwd_tf / peak,
                          "launches": fwd_n, "avg_ms": fwd_avg},
         "exchange": exchange,
