@@ -161,3 +161,27 @@ def test_product_path_does_not_import_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.lower(), f
+
+
+def test_chunk_table_random_splits():
+    """Random (S, P): the library's chunk table is numpy's array_split, and
+    every workspace size covers the backward's fixed parts."""
+    hyp = pytest.importorskip("hypothesis")
+    st = hyp.strategies
+
+    @hyp.settings(max_examples=200, deadline=None)
+    @hyp.given(S=st.integers(1, 200000), P=st.integers(1, 64))
+    def check(S, P):
+        if P > S:
+            return
+        assert ctx.chunk_offsets(S, P) == oracle.chunk_offsets(S, P)
+
+    check()
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_workspace_grows_with_the_problem(lib, D):
+    sizes = [lib.ctx_attn_workspace_size(1, S, 8, 2, D, 4, 0) for S in (512, 1024, 4096, 16384)]
+    assert all(a < b for a, b in zip(sizes, sizes[1:]))
+    assert lib.ctx_attn_workspace_size(2, 4096, 8, 2, D, 4, 0) > sizes[2]
+

@@ -79,3 +79,19 @@ def test_noalloc_refuses_problems_beyond_its_scratch(lib):
     assert rc == 3  # CTX_ERR_WORKSPACE
     need = lib.ctx_attn_workspace_size(1, 32760, 24, 24, 128, 8, 0)
     assert need > 64 * 1024 * 1024
+
+
+def test_noalloc_backward_d256_group_split(lib):
+    """Head dimension 256 at 1024 tokens: the backward splits each GQA group
+    over CTAs and keeps their partial dK/dV in the scratch as well."""
+    sh = AttnShape(B=1, S=1024, Hq=24, Hkv=4, D=256, P=2)
+    assert lib.ctx_attn_workspace_size(1, 1024, 24, 4, 256, 2, 0) <= 64 * 1024 * 1024
+    q, k, v, do = (t.cuda() for t in attn_inputs(sh, seed=32))
+    out, lse = ctx.attn_fwd(q, k, v, sh.P)
+    ref = ctx.attn_bwd(q, k, v, out, lse, do, sh.P)
+    rc, got = _noalloc(lib, q, k, v, out, lse, do, sh.P)
+    assert rc == 0, ctx._status_text(rc)
+    torch.cuda.synchronize()
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        _close(g, r, name)
+    assert ctx.device_status() == 0
