@@ -49,6 +49,11 @@ SMALL = [
     AttnShape(B=2, S=37, Hq=4, Hkv=4, D=16, P=1, layout="bshd"),
     AttnShape(B=1, S=29, Hq=6, Hkv=2, D=8, P=1, layout="bshd"),
     AttnShape(B=2, S=23, Hq=4, Hkv=1, D=16, P=1, layout="sbhd"),
+    # the head dimensions the kernels implement, at the GQA group size of the
+    # 24/4-head model
+    AttnShape(B=1, S=33, Hq=6, Hkv=1, D=64, P=1, layout="bshd"),
+    AttnShape(B=1, S=21, Hq=6, Hkv=1, D=128, P=1, layout="sbhd"),
+    AttnShape(B=1, S=17, Hq=6, Hkv=1, D=256, P=1, layout="bshd"),
 ]
 
 
