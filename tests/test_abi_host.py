@@ -185,3 +185,19 @@ def test_workspace_grows_with_the_problem(lib, D):
     assert all(a < b for a, b in zip(sizes, sizes[1:]))
     assert lib.ctx_attn_workspace_size(2, 4096, 8, 2, D, 4, 0) > sizes[2]
 
+
+
+def test_missing_library_fails_loudly():
+    """No CPU path: without the compiled library every entry point raises."""
+    code = (
+        "import context_attention_fwd_gb300 as ctx, context_attention_fwd_gb300.build as b\n"
+        "b.LIB = '/nonexistent/libctxattn.so'\n"
+        "try:\n"
+        "    ctx.load_library(build_if_missing=False)\n"
+        "except RuntimeError as e:\n"
+        "    print('raised', e)\n"
+    )
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=ROOT, timeout=120)
+    assert r.returncode == 0 and r.stdout.startswith("raised"), r.stdout + r.stderr
