@@ -16,6 +16,9 @@
 //     the full 256-column contraction; TMEM is then S^T, dP^T (later dQ_h),
 //     dV_h, dK_h = 4 x 128 columns as in the D = 128 kernel.  K stays
 //     resident; Q, V and dO stream through a ring of 32 KB column-half slots.
+//     Short sequences give few KV tiles, so the query heads of a GQA group
+//     may further be split over hsplit CTAs, which then write fp32 partial
+//     dK/dV rows for a separate summing kernel.
 #include "internal.h"
 #include "ptx.cuh"
 #include "walk.cuh"
