@@ -250,6 +250,21 @@ def measure_d256(ctx, dev, stream, barrier, peaks):
         if ctx.device_status() != 0:
             raise RuntimeError("device-side wait timed out (D=256)")
         ms = e0.elapsed_time(e1) / reps
+        # the same step captured once in a CUDA graph and replayed (no
+        # per-launch host overhead: matters at 1024 tokens)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        graph.replay()
+        barrier()
+        e0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(stream)
+        barrier()
+        if ctx.device_status() != 0:
+            raise RuntimeError("device-side wait timed out (D=256, graph)")
+        ms_graph = e0.elapsed_time(e1) / reps
         pairs = sh.B * sh.Hq * sh.S * (sh.S + 1) / 2.0
         fl_f, fl_b = 4.0 * pairs * sh.D, 10.0 * pairs * sh.D
         f_ms, f_n = ctx.profile_read("fwd")
@@ -258,6 +273,7 @@ def measure_d256(ctx, dev, stream, barrier, peaks):
         res.append({"workload": name, "B": sh.B, "S": sh.S, "Hq": sh.Hq, "Hkv": sh.Hkv, "D": sh.D,
                     "P": sh.P, "causal": True, "ms_per_step": ms,
                     "value": (fl_f + fl_b) / (ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                    "graph": {"ms_per_step": ms_graph, "value": (fl_f + fl_b) / (ms_graph / 1e3) / 1e12},
                     "fwd_kernel": {"kernel": "attn_fwd256_kernel", "avg_ms": f_avg,
                                    "achieved": fl_f / (f_avg / 1e3) / 1e12,
                                    "frac": fl_f / (f_avg / 1e3) / 1e12 / peaks["bf16"]},
@@ -265,7 +281,7 @@ def measure_d256(ctx, dev, stream, barrier, peaks):
                                    "achieved": fl_b / (b_avg / 1e3) / 1e12,
                                    "frac": fl_b / (b_avg / 1e3) / 1e12 / peaks["bf16"]},
                     "peak": peaks["bf16"], "peak_kind": f"bf16 dense, burst ({peaks['source']})"})
-        del q, k, v, do, out, lse, ws, dq, dk, dv
+        del q, k, v, do, out, lse, ws, dq, dk, dv, graph
     return res
 
 
