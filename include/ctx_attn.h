@@ -20,7 +20,10 @@
  *  - Device memory (inputs, outputs, workspace) is allocated and owned by the
  *    caller.  The library allocates nothing and frees nothing.
  *  - Work is enqueued on the caller's stream and is asynchronous; no entry
- *    point synchronises except ctx_get_device_status.
+ *    point synchronises except ctx_get_device_status.  With the workspace
+ *    and outputs given, a call may be captured in a CUDA graph (after one
+ *    uncaptured call with the same head dimension, which sets the kernels'
+ *    shared-memory attributes).
  *  - Arguments are validated before anything is launched; an invalid call
  *    returns an error code and writes nothing (never a silent wrong result).
  *  - Element type: bf16 for q, k, v, out, dout, dq, dk, dv; fp32 for lse.
@@ -38,8 +41,8 @@
  *  - Scale: scale <= 0 selects 1/sqrt(D).
  *  - causal != 0: key j is visible to query i iff j <= i (global row
  *    indices).  KV chunks after a query chunk are skipped entirely, the
- *    diagonal chunk is masked per element.  The pages' workloads are not
- *    causal; the definition is the usual one.
+ *    diagonal chunk is masked per element.  The diffusion workloads are not
+ *    causal, the D = 256 language model is; the definition is the usual one.
  */
 #ifndef CTX_ATTN_H
 #define CTX_ATTN_H
