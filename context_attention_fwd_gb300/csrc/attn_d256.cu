@@ -62,7 +62,11 @@ struct F256Bars {
     uint64_t q_full;
     uint64_t full[F256::SLOTS], empty[F256::SLOTS];
     uint64_t s_full[2];  // S buffer b holds S(j) for j = b mod 2
-    uint64_t p_full;     // P(j) (and any O rescale) written by the softmax threads
+    // P(j) (and any O rescale) written by the softmax threads, one barrier per
+    // score buffer: with S(j+1) already computed, the softmax may finish tile
+    // j+1 before the issuer has waited for tile j, so a single barrier could
+    // complete two phases and its parity would no longer identify tile j
+    uint64_t p_full[2];
     uint64_t pv_done;    // one completion per PV product
     uint64_t o_done;     // the last PV of a chunk (partials) or of the walk
     uint64_t drain;
@@ -101,7 +105,8 @@ __global__ void __launch_bounds__(kF256Threads, 1) attn_fwd256_kernel(const __gr
         }
         mbar_init(smem_u32(&bars.s_full[0]), 1);
         mbar_init(smem_u32(&bars.s_full[1]), 1);
-        mbar_init(smem_u32(&bars.p_full), 128);  // every softmax thread
+        mbar_init(smem_u32(&bars.p_full[0]), 128);  // every softmax thread
+        mbar_init(smem_u32(&bars.p_full[1]), 128);
         mbar_init(smem_u32(&bars.pv_done), 1);
         mbar_init(smem_u32(&bars.o_done), 1);
         mbar_init(smem_u32(&bars.drain), 1);
@@ -189,7 +194,7 @@ __global__ void __launch_bounds__(kF256Threads, 1) attn_fwd256_kernel(const __gr
             for (int j = 0; j < n_kv && ok; ++j, kv_next(ct, g, w)) {
                 const bool first_c = w.t == w.t0, last_c = w.t == w.t1 - 1;
                 const bool acc0 = kPartials ? !first_c : j > 0;
-                if (!(ok = mbar_wait(smem_u32(&bars.p_full), j & 1, wc))) break;
+                if (!(ok = mbar_wait(smem_u32(&bars.p_full[j & 1]), (j >> 1) & 1, wc))) break;
                 tc_fence_after();
                 const int n0 = j * L::LOADS + 2;
                 const uint32_t pa = tmem + L::TM_S + (j & 1) * 128;  // P(j), bf16 pairs
@@ -307,7 +312,7 @@ __global__ void __launch_bounds__(kF256Threads, 1) attn_fwd256_kernel(const __gr
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(smem_u32(&bars.p_full));
+            mbar_arrive(smem_u32(&bars.p_full[j & 1]));
             if (kPartials && w.t == w.t1 - 1) {  // (no causal masking with partials)
                 const int it = w.it;
                 if (!(ok = mbar_wait(smem_u32(&bars.o_done), it & 1, wc))) break;
