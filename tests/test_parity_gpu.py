@@ -32,6 +32,11 @@ def _lib():
 def check(name, got, ref, tol=TOL):
     g, r = got.double().cpu(), ref.double().cpu()
     assert torch.isfinite(g).all(), f"{name}: non-finite values"
+    if r.abs().max().item() == 0:
+        # an identically zero reference (one key: dq = dk = 0 exactly) has no
+        # relative error; the kernels' fp32 arithmetic leaves rounding noise
+        assert g.abs().max().item() < 1e-3, f"{name}: {g.abs().max().item():.3e} against exact zero"
+        return 0.0, 0.0
     nrm = ((g - r).norm() / r.norm()).item()
     mx = ((g - r).abs().max() / r.abs().max()).item()
     assert nrm <= tol and mx <= tol, f"{name}: norm-rel {nrm:.3e}, max-rel {mx:.3e}"

@@ -1,0 +1,42 @@
+"""A seeded sweep of random small problems against the fp64 oracle: head
+dimension, GQA ratio, batch, length, number of chunks (including explicit
+uneven offsets), storage order and causal masking all drawn at random, so
+that combinations no hand-written case names are covered too."""
+import random
+
+import pytest
+import torch
+
+import context_attention_fwd_gb300 as ctx
+from seeded_inputs import AttnShape
+from test_parity_gpu import check_full, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _cases(n=36, seed=2024):
+    rng = random.Random(seed)
+    out = []
+    for i in range(n):
+        D = rng.choice([64, 128, 256])
+        Hkv = rng.choice([1, 2, 4])
+        Hq = Hkv * rng.choice([1, 2, 3])
+        B = rng.choice([1, 1, 2])
+        S = rng.randint(1, 700 if D < 256 else 520)
+        P = rng.randint(1, min(S, 9))
+        layout = rng.choice(["bshd", "sbhd"])
+        causal = rng.random() < 0.4
+        offsets = None
+        if P > 1 and rng.random() < 0.3:  # explicit uneven chunking
+            cuts = sorted(rng.sample(range(1, S), P - 1))
+            offsets = [0] + cuts + [S]
+        out.append((i, AttnShape(B=B, S=S, Hq=Hq, Hkv=Hkv, D=D, P=P, layout=layout), causal, offsets))
+    return out
+
+
+@pytest.mark.parametrize("i,shape,causal,offsets", _cases(), ids=lambda v: str(v) if isinstance(v, int) else None)
+def test_random_problem_matches_oracle(i, shape, causal, offsets):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ctx.load_library(build_if_missing=True)
+    check_full(*run_gpu(shape, offsets=offsets, causal=causal), causal=causal)
