@@ -34,7 +34,24 @@ def _cases(n=36, seed=2024):
     return out
 
 
-@pytest.mark.parametrize("i,shape,causal,offsets", _cases(), ids=lambda v: str(v) if isinstance(v, int) else None)
+def _longer_cases(n=24, seed=77):
+    """Fewer heads, longer sequences: several tiles per chunk, ragged tails."""
+    rng = random.Random(seed)
+    out = []
+    for i in range(n):
+        D = rng.choice([64, 128, 256])
+        Hkv = rng.choice([1, 2])
+        Hq = Hkv * rng.choice([1, 2])
+        S = rng.randint(700, 2600 if D < 256 else 1600)
+        P = rng.randint(1, 12)
+        causal = rng.random() < 0.4
+        out.append((100 + i, AttnShape(B=1, S=S, Hq=Hq, Hkv=Hkv, D=D, P=P, layout=rng.choice(["bshd", "sbhd"])),
+                    causal, None))
+    return out
+
+
+@pytest.mark.parametrize("i,shape,causal,offsets", _cases() + _longer_cases(),
+                         ids=lambda v: str(v) if isinstance(v, int) else None)
 def test_random_problem_matches_oracle(i, shape, causal, offsets):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
