@@ -31,7 +31,8 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from seeded_inputs import GQA_D256_S1024, VIDEO_S32760_P8, AttnShape, attn_inputs, exchange_input  # noqa: E402
+from seeded_inputs import (GQA_D256_S1024, HYBRID_RING, HYBRID_S65536, HYBRID_ULYSSES,  # noqa: E402
+                           VIDEO_S32760_P8, AttnShape, attn_inputs, exchange_input)
 
 METRIC = "fwd+bwd attention TFLOP/s at 1 GB300 (ring P chunks), % of dense bf16 peak"
 UNIT = "TFLOP/s"
@@ -285,6 +286,58 @@ def measure_d256(ctx, dev, stream, barrier, peaks):
     return res
 
 
+def measure_hybrid(ctx, dev, stream, barrier, steps=2):
+    """The ring 4 x ulysses 2 hybrid at full size, one step = the exchange of
+    q, k, v ([1,65536,32,128], k and v with 8 heads), GQA 32/8 ring attention
+    over 4 chunks on the exchanged tensors (forward and backward, both head
+    groups in one call each), the exchange of dout and the inverse exchange
+    of out, dq, dk, dv.  TFLOP/s over the attention's algorithmic flops."""
+    sh, R, U = HYBRID_S65536, HYBRID_RING, HYBRID_ULYSSES
+    q, k, v, do = (t.to(dev) for t in attn_inputs(sh))
+    W = R * U
+    Ssh = -(-sh.S // W)
+    offs = [min(r * U * Ssh, sh.S) for r in range(R)] + [sh.S]  # rank (r, u) holds these rows
+    ex = [torch.empty(ctx.exchanged_shape(sh.B, sh.S, t.shape[2], sh.D, R, U, "bshd"), dtype=t.dtype, device=dev)
+          for t in (q, k, v, do)]
+    views = [ctx.exchanged_view(t, sh.S, "bshd") for t in ex]
+    vq, vk, vv, vdo = views
+    out, lse = ctx.attn_fwd(vq, vk, vv, R, chunk_offsets=offs)
+    dq, dk, dv = ctx.attn_bwd(vq, vk, vv, out, lse, vdo, R, chunk_offsets=offs)
+    ws = torch.empty(ctx.workspace_size(U * sh.B, sh.S, sh.Hq // U, sh.Hkv // U, sh.D, R), dtype=torch.uint8,
+                     device=dev)
+    back = [torch.empty_like(t) for t in (q, q, k, v)]
+    assert sh.S % W == 0  # no padding rows: the attention's outputs are the dense exchanged layout
+    grp = lambda t: t.view(U, sh.B, sh.S, t.shape[2], sh.D)
+
+    def step():
+        for x, y in zip((q, k, v), ex[:3]):
+            ctx.seq_head_exchange(x, R, U, 0, "bshd", y=y)
+        ctx.attn_fwd(vq, vk, vv, R, chunk_offsets=offs, out=out, lse=lse)
+        ctx.seq_head_exchange(grp(out), R, U, 1, "bshd", y=back[0], S=sh.S, B=sh.B, H=sh.Hq)
+        ctx.seq_head_exchange(do, R, U, 0, "bshd", y=ex[3])
+        ctx.attn_bwd(vq, vk, vv, out, lse, vdo, R, chunk_offsets=offs, dq=dq, dk=dk, dv=dv, workspace=ws)
+        for g_, y, H in ((dq, back[1], sh.Hq), (dk, back[2], sh.Hkv), (dv, back[3], sh.Hkv)):
+            ctx.seq_head_exchange(grp(g_), R, U, 1, "bshd", y=y, S=sh.S, B=sh.B, H=H)
+
+    step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    barrier()
+    if ctx.device_status() != 0:
+        raise RuntimeError("device-side wait timed out (hybrid)")
+    ms = e0.elapsed_time(e1) / steps
+    flops = flops_fwd(sh) + flops_bwd(sh)
+    res = {"workload": "ring 4 x ulysses 2 hybrid, [1,65536,32,128] (k, v 8 heads), GQA 32/8, P=4",
+           "ms_per_step": ms, "value": flops / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "steps": steps,
+           "exchanges_per_step": 8}
+    del q, k, v, do, ex, views, out, lse, dq, dk, dv, ws, back
+    return res
+
+
 def measure_e2e(ctx, dev, sh, host_inputs, ws, steps, barrier, world):
     """End to end through the public API: every step copies that step's
     inputs (q, k, v, dout) from pinned host memory to the GPU, runs the
@@ -366,6 +419,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-exchange", action="store_true")
     ap.add_argument("--no-d256", action="store_true")
+    ap.add_argument("--no-hybrid", action="store_true")
     ap.add_argument("--shape", default=None,
                     help="S,Hq,Hkv,D,P: a smaller case of the same kernels (profiler captures)")
     args = ap.parse_args()
@@ -459,6 +513,11 @@ def main():
     if not args.no_exchange:
         exchange = measure_exchange(ctx, dev, stream, barrier, peaks)
 
+    # ------------------------------------------------ the ring x ulysses hybrid at full size
+    hybrid = None
+    if not args.no_hybrid and not args.shape:
+        hybrid = measure_hybrid(ctx, dev, stream, barrier)
+
     # ------------------------------------------------ head dimension 256 (GQA 24/4, causal)
     d256 = None
     if not args.no_d256:
@@ -483,6 +542,7 @@ def main():
                          "launches": fwd_n, "avg_ms": fwd_avg},
         "exchange": exchange,
         "d256": d256,
+        "hybrid": hybrid,
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
