@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(kF256Threads, 1) attn_fwd256_kernel(const __gr
             KvWalk w;
             kv_first(ct, g, w);
             for (int j = 0; j < n_kv && ok; ++j, kv_next(ct, g, w)) {
-                const bool first_c = w.t == w.t0, last_c = w.t == w.t1 - 1;
+                const bool first_c = w.t == w.t0, last_c = kv_chunk_last(ct, g, w);
                 const bool acc0 = kPartials ? !first_c : j > 0;
                 if (!(ok = mbar_wait(smem_u32(&bars.p_full[j & 1]), (j >> 1) & 1, wc))) break;
                 tc_fence_after();
@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(kF256Threads, 1) attn_fwd256_kernel(const __gr
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(smem_u32(&bars.p_full[j & 1]));
-            if (kPartials && w.t == w.t1 - 1) {  // (no causal masking with partials)
+            if (kPartials && kv_chunk_last(ct, g, w)) {
                 const int it = w.it;
                 if (!(ok = mbar_wait(smem_u32(&bars.o_done), it & 1, wc))) break;
                 tc_fence_after();

@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             tmem_st_wait();
             tc_fence_before();
             group_sync(1 + x);  // every P (and O rescale) of this tile is in TMEM
-            const bool first_c = w.t == w.t0, last_c = w.t == w.t1 - 1;
+            const bool first_c = w.t == w.t0, last_c = kv_chunk_last(ct, g, w);
             if (issuer) {
                 tc_fence_after();
                 const int st = j & 1, st1 = (j + 1) & 1;
@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 }
             }
             __syncwarp();
-            if (partials && last_c) {  // (no causal masking with partials)
+            if (partials && last_c) {
                 // this chunk's partial is complete: O_it / l, LSE_it
                 const int it = w.it;
                 if (!(ok = mbar_wait(o_done, it & 1, wc))) break;

@@ -275,10 +275,14 @@ __global__ void dkv_reduce_kernel(const float* __restrict__ part, int hs, int B,
 
 // LSE merge of materialised partials: L = log sum_i exp(LSE_i),
 // O = sum_i exp(LSE_i - L) O_i.  part_o [P][B][H][S][D], part_lse [P][B][H][S].
-// One thread per 4 columns of a row.
+// With causal masking a row of chunk r has partials for iterations 0..r only
+// (ring order: chunks r, r-1, .., 0; all-gather order: chunks 0..r); the
+// later iterations meet chunks after r, whose weight is zero (LSE = -inf),
+// and are never written.  One thread per 4 columns of a row.
 __global__ void lse_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
                                  int P, int B, int H, int S, int D, __nv_bfloat16* __restrict__ out,
-                                 int64_t osb, int64_t oss, int64_t osh, float* __restrict__ lse) {
+                                 int64_t osb, int64_t oss, int64_t osh, float* __restrict__ lse,
+                                 const ChunkTable ct, int causal) {
     const int g4 = D / 4;
     const int64_t nrows = (int64_t)B * H * S;
     const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -288,13 +292,19 @@ __global__ void lse_merge_kernel(const float* __restrict__ part_o, const float* 
     const int s = (int)(row % S);
     const int64_t bh = row / S;
     const int h = (int)(bh % H), b = (int)(bh / H);
+    int n_it = P;
+    if (causal) {
+        int r = 0;
+        while (r + 1 < ct.P && ct.off[r + 1] <= s) ++r;
+        n_it = r + 1;
+    }
     float m = -INFINITY;
-    for (int i = 0; i < P; ++i) m = fmaxf(m, part_lse[i * nrows + row]);
+    for (int i = 0; i < n_it; ++i) m = fmaxf(m, part_lse[i * nrows + row]);
     float sum = 0.f;
-    for (int i = 0; i < P; ++i) sum += __expf(part_lse[i * nrows + row] - m);
+    for (int i = 0; i < n_it; ++i) sum += __expf(part_lse[i * nrows + row] - m);
     const float L = m + __logf(sum);
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = 0; i < P; ++i) {
+    for (int i = 0; i < n_it; ++i) {
         const float w = __expf(part_lse[i * nrows + row] - L);
         const float4 pi = *reinterpret_cast<const float4*>(part_o + (i * nrows + row) * D + k4 * 4);
         o.x = fmaf(w, pi.x, o.x);
@@ -437,7 +447,6 @@ int ctx_attn_fwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
         return CTX_ERR_INVALID_ARG;
     if (!sizes_ok((int)B, (int)S, (int)Hq, (int)Hkv, (int)D)) return CTX_ERR_INVALID_ARG;
     if (D != 64 && D != 128 && D != 256) return CTX_ERR_UNSUPPORTED;
-    if (causal && (flags & CTX_FLAG_MATERIALIZE_PARTIALS)) return CTX_ERR_UNSUPPORTED;
     Dense dq_, dk_, dv_, do_;
     int rc;
     if ((rc = resolve(q, B, S, Hq, D, layout, &dq_))) return rc;
@@ -484,7 +493,7 @@ int ctx_attn_fwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
         const int blk = 256;
         lse_merge_kernel<<<(unsigned)((threads + blk - 1) / blk), blk, 0, s>>>(
             p.part_o, p.part_lse, P, (int)B, (int)Hq, (int)S, (int)D, p.out, p.o_sb, p.o_ss, p.o_sh,
-            lse);
+            lse, p.ct, p.causal);
         if ((rc = launch_status())) return rc;
     }
     return CTX_OK;

@@ -42,6 +42,14 @@ __device__ __forceinline__ void kv_next(const ChunkTable& ct, const WalkCfg& g, 
     do kv_adv(ct, g, w);
     while (w.it < g.P && !kv_visible(ct, g, w));
 }
+// The visited tile is the last one the walk visits in its chunk (the end of
+// that chunk's partial): the chunk's last tile, or with causal masking in the
+// query chunk itself the last tile starting at or before the CTA's last row.
+__device__ __forceinline__ bool kv_chunk_last(const ChunkTable& ct, const WalkCfg& g, const KvWalk& w) {
+    int last = w.t1 - 1;
+    if (g.causal && w.c == g.r) last = min(last, w.t0 + ((g.q_last - ct.off[w.c]) >> 7));
+    return w.t == last;
+}
 // Number of KV tiles the walk visits.
 __device__ __forceinline__ int kv_count(const ChunkTable& ct, const WalkCfg& g) {
     if (!g.causal) return ct.ntiles;

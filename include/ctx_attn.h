@@ -63,7 +63,7 @@ typedef enum { CTX_LAYOUT_BSHD = 0, CTX_LAYOUT_SBHD = 1 } ctx_layout_t;
 typedef enum {
     CTX_OK = 0,
     CTX_ERR_INVALID_ARG = 1, /* a size, pointer, stride or offset is invalid */
-    CTX_ERR_UNSUPPORTED = 2, /* valid but not implemented (D, causal, alignment) */
+    CTX_ERR_UNSUPPORTED = 2, /* valid but not implemented (D, alignment) */
     CTX_ERR_WORKSPACE = 3,   /* workspace missing, too small or misaligned */
     CTX_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
     CTX_ERR_TIMEOUT = 5      /* a device-side wait ran out of time (see ctx_get_device_status) */
@@ -84,7 +84,9 @@ typedef struct {
 #define CTX_FLAG_NONE 0
 /* Write each ring iteration's partial (O_i, LSE_i) to the workspace and merge
  * them with a separate LSE-merge kernel, instead of merging online inside
- * the attention kernel.  Same result up to fp32 rounding order. */
+ * the attention kernel.  Same result up to fp32 rounding order.  With causal
+ * masking the iterations that meet chunks after the query's own have zero
+ * weight (LSE = -inf) and are neither computed nor merged. */
 #define CTX_FLAG_MATERIALIZE_PARTIALS 1
 /* Visit the KV chunks in the order 0..P-1 (the K/V all-gather pattern of
  * diffusers PR #12443 "Fix Flux Context Parallel Bug ...": every query shard
@@ -106,9 +108,8 @@ int ctx_chunk_offsets(int S, int P, int* offsets_out);
  *   out [B,S,Hq,D] (bf16, written), lse [B,Hq,S] fp32 contiguous (written):
  *   lse = natural-log log-sum-exp of the scaled scores over all S keys.
  * P ring chunks (1 <= P <= min(S, 64)).  workspace may be NULL unless
- * CTX_FLAG_MATERIALIZE_PARTIALS is set (not combined with causal masking:
- * CTX_ERR_UNSUPPORTED).  Output rows are written once; out must not alias
- * q, k or v. */
+ * CTX_FLAG_MATERIALIZE_PARTIALS is set.  Output rows are written once; out
+ * must not alias q, k or v. */
 int ctx_attn_fwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_t* v, int P,
                  const int* chunk_offsets, ctx_layout_t layout, int causal, float scale,
                  const ctx_tensor_t* out, float* lse, void* workspace, size_t workspace_bytes,

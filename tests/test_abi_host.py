@@ -114,7 +114,7 @@ def test_invalid_arguments_fail_before_launch(lib):
     assert call(lse=None) == 1
     assert call(q=_t(fake, 1, 64, 4, 96), k=_t(fake, 1, 64, 2, 96), v=_t(fake, 1, 64, 2, 96),
                 out=_t(fake, 1, 64, 4, 96)) == 2        # D = 96 unsupported
-    assert call(causal=1, flags=1) == 2                 # causal with materialised partials
+    assert call(causal=1, flags=1) == 3                 # causal with materialised partials: needs a workspace
     assert call(out=_t(fake, 1, 63, 4, 64)) == 1        # shape mismatch
     assert call(q=_t(fake + 2, 1, 64, 4, 64)) == 2      # misaligned for TMA
     assert call(flags=1) == 3                           # partials need a workspace

@@ -204,12 +204,21 @@ def test_causal_layouts_and_edges(S, P, layout, offsets):
     check_full(*run_gpu(sh, offsets=offsets, causal=True), causal=True)
 
 
-def test_causal_partials_refused():
-    sh = AttnShape(B=1, S=256, Hq=2, Hkv=2, D=64, P=2)
-    q, k, v, _ = (t.cuda() for t in attn_inputs(sh))
-    with pytest.raises(ctx.CtxError) as e:
-        ctx.attn_fwd(q, k, v, 2, causal=True, flags=ctx.FLAG_MATERIALIZE_PARTIALS)
-    assert e.value.code == 2
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("allgather", [False, True])
+def test_causal_materialized_partials(D, allgather):
+    """Causal masking with materialised partials: per-chunk partials (the
+    query's own chunk ends at its diagonal tile) merged over the iterations
+    that meet chunks at or before the query's; equals the online merge and
+    the oracle."""
+    sh = AttnShape(B=1, S=1001, Hq=4, Hkv=2, D=D, P=4)
+    flags = ctx.FLAG_MATERIALIZE_PARTIALS | (ctx.FLAG_KV_ALLGATHER if allgather else 0)
+    inputs, outputs = run_gpu(sh, flags=flags, causal=True)
+    check_full(inputs, outputs, causal=True)
+    q, k, v, _ = (t.cuda() for t in inputs)
+    o_online, l_online = ctx.attn_fwd(q, k, v, sh.P, causal=True)
+    check("partials vs online", outputs[0], o_online, tol=1e-2)
+    assert (outputs[1] - l_online).abs().max().item() < 1e-4
 
 
 @pytest.mark.parametrize("causal", [False, True])
