@@ -262,3 +262,42 @@ def test_timeout_selftest_reports_status():
     # the context is still usable
     sh = AttnShape(B=1, S=300, Hq=2, Hkv=2, D=64, P=2)
     check_full(*run_gpu(sh))
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_gqa_equals_mha_with_repeated_kv(D):
+    """GQA reads kv head h // (Hq/Hkv): running MHA on K/V with each kv head
+    repeated for its query heads gives the same forward bit for bit, and the
+    GQA dk/dv equal the group sums of the MHA dk/dv."""
+    sh = AttnShape(B=1, S=900, Hq=6, Hkv=2, D=D, P=3)
+    q, k, v, do = (t.cuda() for t in attn_inputs(sh))
+    G = sh.Hq // sh.Hkv
+    k_rep, v_rep = k.repeat_interleave(G, dim=2), v.repeat_interleave(G, dim=2)
+    o_g, l_g = ctx.attn_fwd(q, k, v, sh.P)
+    o_m, l_m = ctx.attn_fwd(q, k_rep, v_rep, sh.P)
+    assert torch.equal(o_g, o_m) and torch.equal(l_g, l_m)
+    dq_g, dk_g, dv_g = ctx.attn_bwd(q, k, v, o_g, l_g, do, sh.P)
+    dq_m, dk_m, dv_m = ctx.attn_bwd(q, k_rep, v_rep, o_m, l_m, do, sh.P)
+    torch.cuda.synchronize()
+    assert ctx.device_status() == 0
+    check("dq", dq_g, dq_m, tol=1e-2)
+    sum_groups = lambda t: t.float().reshape(sh.B, sh.S, sh.Hkv, G, sh.D).sum(dim=3)
+    check("dk", dk_g, sum_groups(dk_m), tol=1e-2)
+    check("dv", dv_g, sum_groups(dv_m), tol=1e-2)
+
+
+@pytest.mark.parametrize("D,scale,causal", [(64, 0.05, False), (128, 0.2, True), (256, 0.03, False)])
+def test_custom_scale(D, scale, causal):
+    """A caller-given softmax scale (instead of 1/sqrt(D)) in both passes."""
+    sh = AttnShape(B=1, S=600, Hq=4, Hkv=2, D=D, P=3)
+    q, k, v, do = attn_inputs(sh)
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    out, lse = ctx.attn_fwd(qd, kd, vd, sh.P, causal=causal, scale=scale)
+    dq, dk, dv = ctx.attn_bwd(qd, kd, vd, out, lse, dod, sh.P, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert ctx.device_status() == 0
+    o_ref, l_ref = oracle.attn_fwd(q, k, v, scale=scale, causal=causal)
+    check("out", out, o_ref)
+    assert (lse.double().cpu() - l_ref).abs().max() < LSE_TOL
+    for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), oracle.attn_bwd(q, k, v, do, scale=scale, causal=causal)):
+        check(name, g, r)
