@@ -146,3 +146,30 @@ def test_hybrid_ring4_ulysses2_full_size_sampled():
     dv_sum = dv.float().sum(dim=1)
     assert ((dv_sum - do_grp).norm() / do_grp.norm()).item() < 2e-2
     assert (dk.float().sum(dim=1).abs().max() / dk.float().abs().sum(dim=1).max()).item() < 2e-2
+
+
+def test_fused_single_call_over_head_group_views():
+    """Fused exchange + attention in one call: a strided view that turns the
+    head group into the batch index ([U, S, H/U, D] for B = 1) runs both
+    groups' attention on the un-exchanged tensors and writes out, dq, dk, dv
+    straight into the un-exchanged layout; equals the explicit pipeline
+    (exchange, attention, inverse exchange) - the forward bit for bit."""
+    sh = AttnShape(B=1, S=4096, Hq=8, Hkv=4, D=128, P=4)
+    ring, U = 4, 2
+    q, k, v, do = (t.cuda() for t in attn_inputs(sh))
+    out_h, dq_h, dk_h, dv_h, offs = hybrid(q, k, v, do, ring=ring, U=U)
+    gview = lambda t, Hg: t[0].view(sh.S, U, Hg, sh.D).permute(1, 0, 2, 3)
+    Hu, Hku = sh.Hq // U, sh.Hkv // U
+    out, dq = torch.empty_like(q), torch.empty_like(q)
+    dk, dv = torch.empty_like(k), torch.empty_like(v)
+    lse = torch.empty(U, Hu, sh.S, dtype=torch.float32, device="cuda")
+    fq, fk, fv, fdo = gview(q, Hu), gview(k, Hku), gview(v, Hku), gview(do, Hu)
+    ctx.attn_fwd(fq, fk, fv, ring, chunk_offsets=offs, out=gview(out, Hu), lse=lse)
+    ctx.attn_bwd(fq, fk, fv, gview(out, Hu), lse, fdo, ring, chunk_offsets=offs,
+                 dq=gview(dq, Hu), dk=gview(dk, Hku), dv=gview(dv, Hku))
+    torch.cuda.synchronize()
+    assert ctx.device_status() == 0
+    assert torch.equal(bits(out), bits(out_h))
+    from test_parity_gpu import check
+    for name, a, b in (("dq", dq, dq_h), ("dk", dk, dk_h), ("dv", dv, dv_h)):
+        check(name, a, b, tol=1e-2)
