@@ -231,16 +231,6 @@ __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Register reallocation between warpgroups (all warps of a warpgroup execute it).
-template <int N>
-__device__ __forceinline__ void regs_inc() {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void regs_dec() {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // ------------------------------------------------------------------ math
 // 2^x on the SFU (PTX ex2.approx, flush-to-zero).
 __device__ __forceinline__ float ex2(float x) {
