@@ -202,6 +202,17 @@ def test_ring_merge_equals_full_attention(S, P):
     assert torch.allclose(l_ring, l_full, rtol=0, atol=1e-12)
 
 
+def test_ring_merge_equals_full_attention_long_sequence():
+    """The long-video workload's chunking (S=32760 as 8 chunks of 4095 rows),
+    on one head with a narrow head dimension to keep the fp64 work small."""
+    sh = AttnShape(B=1, S=32760, Hq=1, Hkv=1, D=8, P=8)
+    q, k, v, _ = attn_inputs(sh, seed=32760)
+    o_full, l_full = oracle.attn_fwd(q, k, v)
+    o_ring, l_ring = oracle.ring_fwd(q, k, v, 8)
+    assert torch.allclose(o_ring, o_full, rtol=0, atol=1e-12)
+    assert torch.allclose(l_ring, l_full, rtol=0, atol=1e-12)
+
+
 def test_ring_merge_custom_offsets_and_causal():
     sh = AttnShape(B=2, S=23, Hq=2, Hkv=2, D=8, P=3)
     q, k, v, do = attn_inputs(sh, seed=1)
