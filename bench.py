@@ -42,8 +42,8 @@ L2_NOTE = "inputs larger than L2 (q/k/v/dout 805 MB vs 126.5 MB L2); no flush"
 
 # dram traffic per launch of the backward kernel from one ncu capture (see
 # profiles/); valid only while the kernel source is the one it was taken on.
-NCU_BWD = {"bytes_per_launch": 1335383040 + 895592448,  # dram read + write, S=32760 H=24 D=128 P=8
-           "source_sha256": "4f0bf6a0924f3ed8193af22c6fb6737b2ede073cb32d68f88aa6e553c2e5812b"}
+NCU_BWD = {"bytes_per_launch": 1333379584 + 891769088,  # dram read + write, S=32760 H=24 D=128 P=8
+           "source_sha256": "3baf3598575a13e3ca1baa4313d321326d8e59a4ef8a88d7326c10300336c076"}
 
 
 def flops_fwd(sh: AttnShape) -> float:

@@ -98,7 +98,7 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                  : "memory");
 }
 
-template <int D>
+template <int D, bool kHeadMajor>
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
     using L = BwdLayout<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -108,7 +108,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                    sDO = sbase + L::OFF_DO, sDS = sbase + L::OFF_DS;
     const float* stat_base = reinterpret_cast<const float*>(smem + L::OFF_STAT);
     const int warp = warp_id(), lane = lane_id();
-    const int kt = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+    const GridPos gp = grid_pos<kHeadMajor>();
+    const int kt = gp.tile, hk = gp.head, b = gp.z;
     const ChunkTable& ct = p.ct;
     const int c = chunk_of_tile(ct, kt);
     const int kv_start = ct.off[c] + (kt - ct.tile_off[c]) * kTile;
@@ -452,15 +453,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     if (warp == kMmaWarp) tmem_dealloc(tmem, L::TM_COLS);
 }
 
-template <int D>
-int launch_bwd_d(const BwdParams& p, cudaStream_t s) {
+template <int D, bool kHeadMajor>
+int launch_bwd_do(const BwdParams& p, cudaStream_t s) {
     using L = BwdLayout<D>;
-    if (cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attn_bwd_kernel<D, kHeadMajor>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::SMEM) != cudaSuccess)
         return 4;
-    dim3 grid(p.ct.ntiles, p.Hkv, p.B);
-    attn_bwd_kernel<D><<<grid, kThreads, L::SMEM, s>>>(p);
+    attn_bwd_kernel<D, kHeadMajor><<<grid_dims(kHeadMajor, p.ct.ntiles, p.Hkv, p.B), kThreads, L::SMEM, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+template <int D>
+int launch_bwd_d(const BwdParams& p, cudaStream_t s) {
+    return p.head_major ? launch_bwd_do<D, true>(p, s) : launch_bwd_do<D, false>(p, s);
 }
 
 }  // namespace

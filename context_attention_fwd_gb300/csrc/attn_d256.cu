@@ -74,7 +74,7 @@ struct F256Bars {
 constexpr int kF256Threads = 256;  // warp 0 loads, warp 1 TMEM + MMA, warps 4..7 softmax
 constexpr float kRescaleThreshold = 8.0f;
 
-template <bool kPartials>
+template <bool kPartials, bool kHeadMajor>
 __global__ void __launch_bounds__(kF256Threads, 1) attn_fwd256_kernel(const __grid_constant__ FwdParams p) {
     using L = F256;
     extern __shared__ uint8_t smem_raw[];
@@ -87,7 +87,8 @@ __global__ void __launch_bounds__(kF256Threads, 1) attn_fwd256_kernel(const __gr
     const int warp = warp_id(), lane = lane_id();
     const ChunkTable& ct = p.ct;
     // the last tiles carry the most work under causal masking: launch them first
-    const int tq = ct.ntiles - 1 - (int)blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const GridPos gp = grid_pos<kHeadMajor>();
+    const int tq = ct.ntiles - 1 - gp.tile, h = gp.head, b = gp.z;
     const int r = chunk_of_tile(ct, tq);
     const int q_start = ct.off[r] + (tq - ct.tile_off[r]) * kTile;
     const int q_rows = min(kTile, ct.off[r + 1] - q_start);
@@ -413,6 +414,7 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 // Load n goes to slot n mod 4 and waits for the release of load n - 4; the
 // releases happen in the order S part A (0), dP part A (1, 2), dK (3),
 // dP part B (4), dV (5), so no load waits on a product that needs it.
+template <bool kHeadMajor>
 __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __grid_constant__ BwdParams p) {
     using L = B256;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -422,8 +424,10 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
     const float* stat_base = reinterpret_cast<const float*>(smem + L::OFF_STAT);
     const int warp = warp_id(), lane = lane_id();
     // z = 2 (b * hsplit + split) + column half
-    const int kt = blockIdx.x, hk = blockIdx.y, hh = blockIdx.z & 1;
-    const int b = (blockIdx.z >> 1) / p.hsplit, split = (blockIdx.z >> 1) % p.hsplit;
+    const GridPos gp = grid_pos<kHeadMajor>();
+    const unsigned z = gp.z;
+    const int kt = gp.tile, hk = gp.head, hh = z & 1;
+    const int b = (z >> 1) / p.hsplit, split = (z >> 1) % p.hsplit;
     const ChunkTable& ct = p.ct;
     const int c = chunk_of_tile(ct, kt);
     const int kv_start = ct.off[c] + (kt - ct.tile_off[c]) * kTile;
@@ -792,20 +796,20 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
 
 int launch_attn_fwd256(const FwdParams& p, cudaStream_t s) {
     const bool partials = p.part_o != nullptr;
-    auto kern = partials ? attn_fwd256_kernel<true> : attn_fwd256_kernel<false>;
+    auto kern = partials ? (p.head_major ? attn_fwd256_kernel<true, true> : attn_fwd256_kernel<true, false>)
+                         : (p.head_major ? attn_fwd256_kernel<false, true> : attn_fwd256_kernel<false, false>);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, F256::SMEM) != cudaSuccess)
         return 4;
-    dim3 grid(p.ct.ntiles, p.Hq, p.B);
-    kern<<<grid, kF256Threads, F256::SMEM, s>>>(p);
+    kern<<<grid_dims(p.head_major, p.ct.ntiles, p.Hq, p.B), kF256Threads, F256::SMEM, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
 
 int launch_attn_bwd256(const BwdParams& p, cudaStream_t s) {
-    if (cudaFuncSetAttribute(attn_bwd256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, B256::SMEM) !=
-        cudaSuccess)
+    auto kern = p.head_major ? attn_bwd256_kernel<true> : attn_bwd256_kernel<false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, B256::SMEM) != cudaSuccess)
         return 4;
-    dim3 grid(p.ct.ntiles, p.Hkv, p.B * 2 * p.hsplit);  // z = 2 (b * hsplit + split) + column half
-    attn_bwd256_kernel<<<grid, kB256Threads, B256::SMEM, s>>>(p);
+    // z = 2 (b * hsplit + split) + column half
+    kern<<<grid_dims(p.head_major, p.ct.ntiles, p.Hkv, p.B * 2 * p.hsplit), kB256Threads, B256::SMEM, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
 

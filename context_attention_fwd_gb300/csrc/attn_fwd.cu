@@ -89,7 +89,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
         if (globaltimer_ns() - t0 > limit_ns) break;
 }
 
-template <int D, bool kPartials>
+template <int D, bool kPartials, bool kHeadMajor>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
     using L = FwdLayout<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -101,7 +101,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const uint32_t sQ = sbase + L::OFF_Q, sK = sbase + L::OFF_K, sV = sbase + L::OFF_V;
     const int warp = warp_id(), lane = lane_id();
     // the last pairs carry the most work under causal masking: launch them first
-    const int pair = p.ct.npairs - 1 - (int)blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const GridPos gp = grid_pos<kHeadMajor>();
+    const int pair = p.ct.npairs - 1 - gp.tile, h = gp.head, b = gp.z;
     const ChunkTable& ct = p.ct;
     const int P = ct.P;
     int r = 0;
@@ -391,15 +392,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     if (warp == 1) tmem_dealloc(tmem, L::TM_COLS);
 }
 
-template <int D, bool kPartials>
-int launch_fwd_dp(const FwdParams& p, cudaStream_t s) {
+template <int D, bool kPartials, bool kHeadMajor>
+int launch_fwd_dpo(const FwdParams& p, cudaStream_t s) {
     using L = FwdLayout<D>;
-    if (cudaFuncSetAttribute(attn_fwd_kernel<D, kPartials>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attn_fwd_kernel<D, kPartials, kHeadMajor>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::SMEM) != cudaSuccess)
         return 4;
-    dim3 grid(p.ct.npairs, p.Hq, p.B);
-    attn_fwd_kernel<D, kPartials><<<grid, kThreads, L::SMEM, s>>>(p);
+    attn_fwd_kernel<D, kPartials, kHeadMajor>
+        <<<grid_dims(kHeadMajor, p.ct.npairs, p.Hq, p.B), kThreads, L::SMEM, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+template <int D, bool kPartials>
+int launch_fwd_dp(const FwdParams& p, cudaStream_t s) {
+    return p.head_major ? launch_fwd_dpo<D, kPartials, true>(p, s) : launch_fwd_dpo<D, kPartials, false>(p, s);
 }
 
 // The materialised-partials code path is a separate instantiation so that

@@ -49,6 +49,17 @@ int num_sms() {
     return n > 0 ? n : 148;
 }
 
+// Launch order of the attention kernels.  Under causal masking the work of
+// a CTA falls off along the tile index, and the kernels launch the heaviest
+// tile of a head first.  On grids of a few waves the order across heads
+// decides the makespan too: in the head-major order (grid (heads, z, tiles))
+// the heaviest tile of every head starts before any lighter one (longest
+// job first).  Larger grids keep the tile-major order (grid (tiles, heads,
+// z)): the CTAs in flight share one head's K/V, which stays hot in L2.
+int pick_head_major(int causal, int64_t ctas) {
+    return causal && ctas <= 4LL * num_sms() ? 1 : 0;
+}
+
 struct Dense {
     void* data;
     int64_t sb, ss, sh;
@@ -475,6 +486,7 @@ int ctx_attn_fwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
     p.group = (int)(Hq / Hkv);
     p.causal = causal ? 1 : 0;
     p.allgather = (flags & CTX_FLAG_KV_ALLGATHER) ? 1 : 0;
+    p.head_major = pick_head_major(p.causal, (int64_t)(D == 256 ? p.ct.ntiles : p.ct.npairs) * Hq * B);
     p.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
     p.scale_log2 = p.scale * 1.4426950408889634f;
     p.out = static_cast<__nv_bfloat16*>(do_.data);
@@ -547,6 +559,7 @@ int ctx_attn_bwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
     p.B = (int)B; p.S = (int)S; p.Hq = (int)Hq; p.Hkv = (int)Hkv;
     p.group = (int)(Hq / Hkv);
     p.causal = causal ? 1 : 0;
+    p.head_major = pick_head_major(p.causal, (int64_t)p.ct.ntiles * Hkv * B * (D == 256 ? 2 * p.hsplit : 1));
     p.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
     p.scale_log2 = p.scale * 1.4426950408889634f;
     p.lse2 = lse2_t;

@@ -48,6 +48,7 @@ struct FwdParams {
     float* part_lse;
     int* status;
     uint64_t timeout_ns;
+    int head_major;  // launch order of the attention kernel (grid_pos in walk.cuh)
 };
 
 struct BwdParams {
@@ -72,6 +73,7 @@ struct BwdParams {
     float* dkv_part;
     int* status;
     uint64_t timeout_ns;
+    int head_major;  // launch order of the attention kernel (grid_pos in walk.cuh)
 };
 
 int launch_attn_fwd(const FwdParams& p, int D, cudaStream_t s);

@@ -12,6 +12,22 @@
 
 namespace ctxattn {
 
+// ------------------------------------------------------------ launch order
+// (tile, head, z) of this CTA: the grid is (tiles, heads, z) in the tile-major
+// order and (heads, z, tiles) in the head-major one, which launches tile 0 of
+// every head before tile 1 of any (the host picks the order per launch).
+struct GridPos {
+    int tile, head, z;
+};
+template <bool kHeadMajor>
+__device__ __forceinline__ GridPos grid_pos() {
+    if (kHeadMajor) return {(int)blockIdx.z, (int)blockIdx.x, (int)blockIdx.y};
+    return {(int)blockIdx.x, (int)blockIdx.y, (int)blockIdx.z};
+}
+inline dim3 grid_dims(bool head_major, int tiles, int heads, int z) {
+    return head_major ? dim3(heads, z, tiles) : dim3(tiles, heads, z);
+}
+
 // ------------------------------------------------------------ forward walk
 struct KvWalk {
     int it, c, t, t0, t1;

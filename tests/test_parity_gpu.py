@@ -204,6 +204,29 @@ def test_causal_layouts_and_edges(S, P, layout, offsets):
     check_full(*run_gpu(sh, offsets=offsets, causal=True), causal=True)
 
 
+def test_causal_many_waves_sampled():
+    """Causal masking on grids of many waves (over four per SM: each head's
+    tiles are launched together); the cases above have grids of a few waves,
+    which are launched heavy tiles of every head first.  Sampled rows at
+    chunk and tile edges against the oracle."""
+    sh = AttnShape(B=2, S=8192, Hq=24, Hkv=8, D=128, P=4)
+    inputs, outputs = run_gpu(sh, causal=True)
+    q, k, v, do = inputs
+    out, lse, dq, dk, dv = outputs
+    off = oracle.chunk_offsets(sh.S, sh.P)
+    edges = sorted({o + d for o in off for d in (-1, 0, 1, 127, 128) if 0 <= o + d < sh.S})
+    rows = [(b, h, s) for b, h, s in zip([0, 1] * 12, [0, 5, 17, 23] * 6, edges[:24])]
+    o_ref, l_ref = oracle.fwd_rows(q, k, v, rows, causal=True)
+    check("out rows", torch.stack([out[b, s, h].cpu() for b, h, s in rows]), o_ref)
+    assert max(abs(lse[b, h, s].item() - l_ref[i].item()) for i, (b, h, s) in enumerate(rows)) < LSE_TOL
+    check("dq rows", torch.stack([dq[b, s, h].cpu() for b, h, s in rows]),
+          oracle.dq_rows(q, k, v, do, rows, causal=True))
+    krows = [(1, 6, s) for s in edges[:12]]
+    dk_ref, dv_ref = oracle.dkv_rows(q, k, v, do, krows, causal=True)
+    check("dk rows", torch.stack([dk[b, s, h].cpu() for b, h, s in krows]), dk_ref)
+    check("dv rows", torch.stack([dv[b, s, h].cpu() for b, h, s in krows]), dv_ref)
+
+
 @pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("allgather", [False, True])
 def test_causal_materialized_partials(D, allgather):
