@@ -50,7 +50,29 @@ def _longer_cases(n=24, seed=77):
     return out
 
 
-@pytest.mark.parametrize("i,shape,causal,offsets", _cases() + _longer_cases(),
+def _causal_grid_cases(n=40, seed=4242):
+    """Mostly causal, up to 48 query heads and batch 3: grids on both sides of
+    the launch-order switch (heads first on small causal grids)."""
+    rng = random.Random(seed)
+    out = []
+    for i in range(n):
+        D = rng.choice([64, 128, 256])
+        Hkv = rng.choice([1, 2, 4, 8])
+        Hq = Hkv * rng.choice([1, 2, 3, 6])
+        B = rng.choice([1, 1, 2, 3])
+        S = rng.randint(1, 1500 if D < 256 else 1100)
+        P = rng.randint(1, min(S, 12))
+        causal = rng.random() < 0.7
+        offsets = None
+        if P > 1 and rng.random() < 0.3:
+            cuts = sorted(rng.sample(range(1, S), P - 1))
+            offsets = [0] + cuts + [S]
+        out.append((200 + i, AttnShape(B=B, S=S, Hq=Hq, Hkv=Hkv, D=D, P=P, layout=rng.choice(["bshd", "sbhd"])),
+                    causal, offsets))
+    return out
+
+
+@pytest.mark.parametrize("i,shape,causal,offsets", _cases() + _longer_cases() + _causal_grid_cases(),
                          ids=lambda v: str(v) if isinstance(v, int) else None)
 def test_random_problem_matches_oracle(i, shape, causal, offsets):
     if not torch.cuda.is_available():
