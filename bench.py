@@ -221,12 +221,19 @@ def measure_exchange(ctx, dev, stream, barrier, peaks):
 def measure_d256(ctx, dev, stream, barrier, peaks):
     """Head dimension 256: the 24/4-head causal language model (1024 tokens,
     P=2; inputs 14 MB, resident in L2) and a long-context case of the same
-    heads (16384 tokens, P=8).  Causal flop count: the S (S + 1) / 2 visible
+    heads (16384 tokens, P=8)."""
+    return measure_causal(ctx, dev, stream, barrier, peaks,
+                          (("24/4-head D=256 causal LM, S=1024, P=2", GQA_D256_S1024, 50),
+                           ("same heads, long context S=16384, P=8",
+                            AttnShape(B=1, S=16384, Hq=24, Hkv=4, D=256, P=8), 5)))
+
+
+def measure_causal(ctx, dev, stream, barrier, peaks, cases):
+    """Causal fwd + bwd steps, eager and replayed from a CUDA graph, with the
+    kernels' own event times.  Causal flop count: the S (S + 1) / 2 visible
     pairs, 4 D flop each forward and 10 D backward, per query head."""
     res = []
-    for name, sh, reps in (("24/4-head D=256 causal LM, S=1024, P=2", GQA_D256_S1024, 50),
-                           ("same heads, long context S=16384, P=8",
-                            AttnShape(B=1, S=16384, Hq=24, Hkv=4, D=256, P=8), 5)):
+    for name, sh, reps in cases:
         q, k, v, do = (t.to(dev) for t in attn_inputs(sh))
         out, lse = ctx.attn_fwd(q, k, v, sh.P, causal=True)
         ws = torch.empty(ctx.workspace_size(sh.B, sh.S, sh.Hq, sh.Hkv, sh.D, sh.P), dtype=torch.uint8,
@@ -249,7 +256,7 @@ def measure_d256(ctx, dev, stream, barrier, peaks):
         barrier()
         ctx.profile_enable(False)
         if ctx.device_status() != 0:
-            raise RuntimeError("device-side wait timed out (D=256)")
+            raise RuntimeError(f"device-side wait timed out ({name})")
         ms = e0.elapsed_time(e1) / reps
         # the same step captured once in a CUDA graph and replayed (no
         # per-launch host overhead: matters at 1024 tokens)
@@ -264,21 +271,23 @@ def measure_d256(ctx, dev, stream, barrier, peaks):
         e1.record(stream)
         barrier()
         if ctx.device_status() != 0:
-            raise RuntimeError("device-side wait timed out (D=256, graph)")
+            raise RuntimeError(f"device-side wait timed out ({name}, graph)")
         ms_graph = e0.elapsed_time(e1) / reps
         pairs = sh.B * sh.Hq * sh.S * (sh.S + 1) / 2.0
         fl_f, fl_b = 4.0 * pairs * sh.D, 10.0 * pairs * sh.D
         f_ms, f_n = ctx.profile_read("fwd")
         b_ms, b_n = ctx.profile_read("bwd")
         f_avg, b_avg = f_ms / max(f_n, 1), b_ms / max(b_n, 1)
+        fname, bname = (("attn_fwd256_kernel", "attn_bwd256_kernel") if sh.D == 256
+                        else (f"attn_fwd_kernel<{sh.D}>", f"attn_bwd_kernel<{sh.D}>"))
         res.append({"workload": name, "B": sh.B, "S": sh.S, "Hq": sh.Hq, "Hkv": sh.Hkv, "D": sh.D,
                     "P": sh.P, "causal": True, "ms_per_step": ms,
                     "value": (fl_f + fl_b) / (ms / 1e3) / 1e12, "unit": "TFLOP/s",
                     "graph": {"ms_per_step": ms_graph, "value": (fl_f + fl_b) / (ms_graph / 1e3) / 1e12},
-                    "fwd_kernel": {"kernel": "attn_fwd256_kernel", "avg_ms": f_avg,
+                    "fwd_kernel": {"kernel": fname, "avg_ms": f_avg,
                                    "achieved": fl_f / (f_avg / 1e3) / 1e12,
                                    "frac": fl_f / (f_avg / 1e3) / 1e12 / peaks["bf16"]},
-                    "bwd_kernel": {"kernel": "attn_bwd256_kernel", "avg_ms": b_avg,
+                    "bwd_kernel": {"kernel": bname, "avg_ms": b_avg,
                                    "achieved": fl_b / (b_avg / 1e3) / 1e12,
                                    "frac": fl_b / (b_avg / 1e3) / 1e12 / peaks["bf16"]},
                     "peak": peaks["bf16"], "peak_kind": f"bf16 dense, burst ({peaks['source']})"})
@@ -460,6 +469,7 @@ def main():
     ap.add_argument("--no-exchange", action="store_true")
     ap.add_argument("--no-d256", action="store_true")
     ap.add_argument("--no-hybrid", action="store_true")
+    ap.add_argument("--no-causal", action="store_true")
     ap.add_argument("--shape", default=None,
                     help="S,Hq,Hkv,D,P: a smaller case of the same kernels (profiler captures)")
     args = ap.parse_args()
@@ -563,6 +573,13 @@ def main():
     if not args.no_d256:
         d256 = measure_d256(ctx, dev, stream, barrier, peaks)
 
+    # ------------------------------------------------ the long-context workload with causal masking
+    causal = None
+    if not args.no_causal and not args.shape:
+        causal = measure_causal(ctx, dev, stream, barrier, peaks,
+                                (("video-DiT shape with causal masking, B=1 S=32760 H=24 D=128, P=8",
+                                  AttnShape(B=1, S=32760, Hq=24, Hkv=24, D=128, P=8), 3),))
+
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
@@ -582,6 +599,7 @@ def main():
                          "launches": fwd_n, "avg_ms": fwd_avg},
         "exchange": exchange,
         "d256": d256,
+        "causal": causal,
         "hybrid": hybrid,
         "e2e": e2e,
     }
