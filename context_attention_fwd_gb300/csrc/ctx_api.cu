@@ -7,7 +7,10 @@
 #include <stdio.h>
 #include <stdlib.h>
 
+#include <algorithm>
+#include <functional>
 #include <mutex>
+#include <vector>
 
 #include "../../include/ctx_attn.h"
 #include "internal.h"
@@ -381,22 +384,82 @@ size_t fwd_ws_bytes(int B, int S, int Hq, int D, int P, int flags) {
     return align256(rows * D * 4) + align256(rows * 4);
 }
 
-// D = 256 backward: CTAs per (KV tile, column half) that share the query
-// heads of one GQA group, chosen so that the grid fills about one wave of a
-// 148..152-SM GPU when the sequence is short.  Non-increasing in ntiles.
-int bwd_hsplit(int64_t ntiles, int B, int Hq, int Hkv, int D) {
+// D = 256 backward on short sequences: the query heads of one GQA group may
+// be split over d CTAs per (KV tile, column half), each writing fp32 partial
+// dK/dV rows that dkv_reduce_kernel sums.  The workspace holds the partial
+// rows of the largest split a call may use: the smallest divisor d of the
+// group size that brings the grid to >= 148 CTAs at the fewest tiles any
+// chunking of S has (ceil(S / 128)).
+int bwd_hsplit_cap(int S, int B, int Hq, int Hkv, int D) {
     if (D != 256) return 1;
     const int G = Hq / Hkv;
-    const int64_t base = ntiles * Hkv * 2 * B;
+    const int64_t base = (int64_t)((S + kTile - 1) / kTile) * Hkv * 2 * B;
     for (int d = 1; d < G; ++d)
         if (G % d == 0 && base * d >= 148) return d;
     return G;
 }
 
+// Estimated time of the D = 256 backward, in query-tile iterations of one
+// CTA, for a split d: the CTAs of KV tile kt each run (query tiles they see)
+// x (G / d) iterations plus about one for their prologue, heaviest first,
+// each on the first SM that is free (list scheduling); summing d partials
+// adds about 0.15 d B Hkv S / 1024.  On the GB300 (24/4 heads, S = 512 ..
+// 2048, causal or not) the split with the smallest estimate was the fastest
+// measured one in every case.
+double bwd_split_time(int64_t nt, int B, int Hkv, int G, int d, int S, int causal, int nsm) {
+    std::vector<double> sm((size_t)nsm, 0.0);  // min-heap of SM finish times
+    const int64_t per_tile = (int64_t)Hkv * 2 * B * d;
+    for (int64_t kt = 0; kt < nt; ++kt) {
+        const double w = (double)((causal ? nt - kt : nt) * (G / d)) + 1.0;
+        for (int64_t j = 0; j < per_tile; ++j) {
+            std::pop_heap(sm.begin(), sm.end(), std::greater<double>());
+            sm.back() += w;
+            std::push_heap(sm.begin(), sm.end(), std::greater<double>());
+        }
+    }
+    const double span = *std::max_element(sm.begin(), sm.end());
+    return span + (d > 1 ? 0.15 * d * B * Hkv * S / 1024.0 : 0.0);
+}
+
+// The split a call uses: the one of smallest estimated time up to the cap
+// (ties to the smaller split).  Memoised: the estimate runs on the host.
+int bwd_hsplit(int64_t ntiles, int S, int B, int Hq, int Hkv, int D, int causal) {
+    const int cap = bwd_hsplit_cap(S, B, Hq, Hkv, D);
+    if (cap == 1) return 1;
+    const int G = Hq / Hkv, nsm = num_sms();
+    struct Entry {
+        int64_t nt;
+        int S, B, Hkv, G, causal, nsm, cap, d;
+    };
+    static std::mutex mu;
+    static Entry memo[32];
+    static int n_memo = 0, next_slot = 0;
+    const Entry key{ntiles, S, B, Hkv, G, causal ? 1 : 0, nsm, cap, 0};
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_memo; ++i) {
+        const Entry& e = memo[i];
+        if (e.nt == key.nt && e.S == key.S && e.B == key.B && e.Hkv == key.Hkv && e.G == key.G &&
+            e.causal == key.causal && e.nsm == key.nsm && e.cap == key.cap)
+            return e.d;
+    }
+    int best = 1;
+    double best_t = 0.0;
+    for (int d = 1; d <= cap; ++d) {
+        if (G % d) continue;
+        const double t = bwd_split_time(ntiles, B, Hkv, G, d, S, causal, nsm);
+        if (d == 1 || t < best_t) best = d, best_t = t;
+    }
+    Entry e = key;
+    e.d = best;
+    memo[next_slot] = e;
+    next_slot = (next_slot + 1) % 32;
+    if (n_memo < 32) ++n_memo;
+    return best;
+}
+
 size_t bwd_ws_bytes(int B, int S, int Hq, int Hkv, int D, int P) {
     const size_t slots = (size_t)B * Hq * ntiles_upper(S, P) * kTile;
-    // every chunking has at least ceil(S / 128) tiles: the largest split
-    const int hs = bwd_hsplit((S + kTile - 1) / kTile, B, Hq, Hkv, D);
+    const int hs = bwd_hsplit_cap(S, B, Hq, Hkv, D);
     const size_t part = hs > 1 ? align256((size_t)hs * B * Hkv * S * 2 * D * 4) : 0;
     return align256(slots * 4) * 2 + align256(slots * D * 4) + part;
 }
@@ -547,7 +610,7 @@ int ctx_attn_bwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
     float* lse2_t = reinterpret_cast<float*>(ws);
     float* delta_t = reinterpret_cast<float*>(ws + align256(slots * 4));
     float* dq_acc = reinterpret_cast<float*>(ws + 2 * align256(slots * 4));
-    p.hsplit = bwd_hsplit(p.ct.ntiles, (int)B, (int)Hq, (int)Hkv, (int)D);
+    p.hsplit = bwd_hsplit(p.ct.ntiles, (int)S, (int)B, (int)Hq, (int)Hkv, (int)D, causal);
     if ((int64_t)B * 2 * p.hsplit > 65535) p.hsplit = 1;  // grid z limit (B <= 32767 checked above)
     p.dkv_part = p.hsplit > 1 ? reinterpret_cast<float*>(ws + 2 * align256(slots * 4) + align256(slots * D * 4))
                               : nullptr;
