@@ -99,15 +99,46 @@ def _check(rc: int, what: str):
         raise CtxError(rc, what)
 
 
-def _desc(t: torch.Tensor) -> _Tensor:
+def _desc(t: torch.Tensor, name: str = "tensor", bits16: bool = False) -> _Tensor:
+    """ctx_tensor_t of a logical [B,S,H,D] tensor.  The C ABI carries no
+    element type (bf16 throughout), so the type is checked here; the
+    exchange (bits16) only moves 16-bit elements and takes any such type."""
     if t.dim() != 4:
-        raise ValueError("expected a logical [B,S,H,D] tensor")
+        raise ValueError(f"{name}: expected a logical [B,S,H,D] tensor, got {t.dim()} dims")
+    if bits16 and t.element_size() != 2:
+        raise ValueError(f"{name}: the exchange moves 16-bit elements, got {t.dtype}")
+    if not bits16 and t.dtype != torch.bfloat16:
+        raise ValueError(f"{name}: dtype must be torch.bfloat16, got {t.dtype}")
     if not t.is_cuda:
-        raise ValueError("tensor must be on a CUDA device")
+        raise ValueError(f"{name}: tensor must be on a CUDA device")
     if t.stride(3) != 1:
-        raise ValueError("the D dimension must be contiguous")
+        raise ValueError(f"{name}: the D dimension must be contiguous")
     B, S, H, D = t.shape
     return _Tensor(t.data_ptr(), B, S, H, D, t.stride(0), t.stride(1), t.stride(2))
+
+
+def _check_types(named):
+    """Ranks and element types of a call's [B,S,H,D] tensors."""
+    for name, t in named:
+        if t.dim() != 4:
+            raise ValueError(f"{name}: expected a logical [B,S,H,D] tensor, got {t.dim()} dims")
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{name}: dtype must be torch.bfloat16, got {t.dtype}")
+
+
+def _check_inputs(named, device, lse=None, lse_shape=None):
+    """A call's tensors before anything is allocated or launched: ranks and
+    element types, the lse buffer, then devices."""
+    _check_types(named)
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != tuple(lse_shape)
+                            or not lse.is_contiguous()):
+        raise ValueError(f"lse: expected a contiguous float32 tensor of shape {tuple(lse_shape)}, "
+                         f"got {lse.dtype} {tuple(lse.shape)}")
+    for name, t in named + ([("lse", lse)] if lse is not None else []):
+        if not t.is_cuda:
+            raise ValueError(f"{name}: tensor must be on a CUDA device")
+        if t.device != device:
+            raise ValueError(f"{name}: on {t.device}, the other tensors are on {device}")
 
 
 def _stream(t: torch.Tensor):
@@ -154,7 +185,10 @@ def attn_fwd(q, k, v, P, chunk_offsets=None, causal=False, scale=None, out=None,
              flags=0, workspace=None):
     """Ring-chunked attention forward -> (out bf16 [B,S,Hq,D] like q, lse fp32 [B,Hq,S])."""
     lib = load_library()
+    named = [("q", q), ("k", k), ("v", v)] + ([("out", out)] if out is not None else [])
+    _check_types(named)
     B, S, Hq, D = q.shape
+    _check_inputs(named, q.device, lse, (B, Hq, S))
     out = _like_layout(q, Hq) if out is None else out
     lse = torch.empty(B, Hq, S, dtype=torch.float32, device=q.device) if lse is None else lse
     nbytes = (lib.ctx_attn_workspace_size(B, S, Hq, k.shape[2], D, P, flags)
@@ -174,8 +208,12 @@ def attn_bwd(q, k, v, out, lse, dout, P, chunk_offsets=None, causal=False, scale
              dq=None, dk=None, dv=None, workspace=None):
     """Ring-chunked attention backward -> (dq, dk, dv) bf16, stored like q / k."""
     lib = load_library()
+    named = [("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)]
+    named += [(n, t) for n, t in (("dq", dq), ("dk", dk), ("dv", dv)) if t is not None]
+    _check_types(named)
     B, S, Hq, D = q.shape
     Hkv = k.shape[2]
+    _check_inputs(named, q.device, lse, (B, Hq, S))
     dq = _like_layout(q, Hq) if dq is None else dq
     dk = _like_layout(k, Hkv) if dk is None else dk
     dv = _like_layout(k, Hkv) if dv is None else dv
@@ -210,8 +248,8 @@ def seq_head_exchange(x, ring, ulysses, direction, layout, y=None, S=None, B=Non
         B_, S_, H_, D = x.shape
         y = torch.empty(exchanged_shape(B_, S_, H_, D, ring, ulysses, layout), dtype=x.dtype,
                         device=x.device) if y is None else y
-        rc = lib.ctx_seq_head_exchange(ctypes.byref(_desc(x)), ctypes.c_void_p(y.data_ptr()), ring,
-                                       ulysses, 0, lay, _stream(x))
+        rc = lib.ctx_seq_head_exchange(ctypes.byref(_desc(x, "x", bits16=True)), ctypes.c_void_p(y.data_ptr()),
+                                       ring, ulysses, 0, lay, _stream(x))
         _check(rc, "ctx_seq_head_exchange")
         return y
     D = x.shape[-1]
@@ -222,8 +260,8 @@ def seq_head_exchange(x, ring, ulysses, direction, layout, y=None, S=None, B=Non
             y = torch.empty(S, B, H, D, dtype=x.dtype, device=x.device).permute(1, 0, 2, 3)
     if not x.is_contiguous():
         raise ValueError("the exchanged buffer must be dense")
-    rc = lib.ctx_seq_head_exchange(ctypes.byref(_desc(y)), ctypes.c_void_p(x.data_ptr()), ring,
-                                   ulysses, 1, lay, _stream(x))
+    rc = lib.ctx_seq_head_exchange(ctypes.byref(_desc(y, "y", bits16=True)), ctypes.c_void_p(x.data_ptr()),
+                                   ring, ulysses, 1, lay, _stream(x))
     _check(rc, "ctx_seq_head_exchange")
     return y
 

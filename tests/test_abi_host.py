@@ -201,3 +201,26 @@ def test_missing_library_fails_loudly():
     import sys
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=ROOT, timeout=120)
     assert r.returncode == 0 and r.stdout.startswith("raised"), r.stdout + r.stderr
+
+
+def test_binding_checks_element_types_before_any_call(lib):
+    """The C ABI carries no element type (bf16 throughout, fp32 lse): the
+    binding refuses other types and host tensors with a ValueError before it
+    allocates or calls anything, so no call can read the wrong bytes."""
+    import torch
+    q32 = torch.zeros(1, 8, 2, 64, dtype=torch.float32)
+    with pytest.raises(ValueError, match="bfloat16"):
+        ctx.attn_fwd(q32, q32, q32, 1)
+    qb = q32.bfloat16()
+    with pytest.raises(ValueError, match="bfloat16"):
+        ctx.attn_fwd(qb, q32.half(), qb, 1)
+    with pytest.raises(ValueError, match="CUDA device"):
+        ctx.attn_fwd(qb, qb, qb, 1)
+    with pytest.raises(ValueError, match="bfloat16"):
+        ctx.attn_bwd(qb, qb, qb, qb, torch.zeros(1, 2, 8), q32, 1)
+    with pytest.raises(ValueError, match="lse"):
+        ctx.attn_bwd(qb, qb, qb, qb, torch.zeros(1, 2, 8, dtype=torch.float64), qb, 1)
+    with pytest.raises(ValueError, match=r"\[B,S,H,D\]"):
+        ctx.attn_fwd(qb[0], qb[0], qb[0], 1)
+    with pytest.raises(ValueError, match="16-bit"):
+        ctx.seq_head_exchange(q32, 2, 1, 0, "bshd")
