@@ -324,3 +324,20 @@ def test_custom_scale(D, scale, causal):
     assert (lse.double().cpu() - l_ref).abs().max() < LSE_TOL
     for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), oracle.attn_bwd(q, k, v, do, scale=scale, causal=causal)):
         check(name, g, r)
+
+
+def test_binding_refuses_wrong_types_on_the_gpu():
+    """Device tensors of another element type, a malformed lse buffer or a
+    host tensor among device ones are refused before any launch."""
+    q = torch.zeros(1, 128, 2, 64, device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="bfloat16"):
+        ctx.attn_fwd(q.half(), q, q, 1)
+    with pytest.raises(ValueError, match="lse"):
+        ctx.attn_fwd(q, q, q, 1, lse=torch.empty(1, 2, 127, device="cuda"))
+    with pytest.raises(ValueError, match="CUDA device"):
+        ctx.attn_fwd(q, q.cpu(), q, 1)
+    out, lse = ctx.attn_fwd(q, q, q, 1)
+    with pytest.raises(ValueError, match="bfloat16"):
+        ctx.attn_bwd(q, q, q, out, lse, q.float(), 1)
+    torch.cuda.synchronize()
+    assert ctx.device_status() == 0
