@@ -188,6 +188,33 @@ def test_video_s32760_p8_full_size_sampled():
     assert (dk.float().sum(dim=1).abs().max() / dk.float().abs().sum(dim=1).max()).item() < 2e-2
 
 
+def test_video_s32760_p8_causal_full_size_sampled():
+    """The long-context shape with causal masking, as the bench times it:
+    sampled rows at chunk and tile edges against the oracle, one head's
+    key rows, and the sum rules (every row's probabilities still sum to
+    one, so they hold under the mask)."""
+    sh = VIDEO_S32760_P8
+    inputs, outputs = run_gpu(sh, causal=True)
+    q, k, v, do = inputs
+    out, lse, dq, dk, dv = outputs
+    off = oracle.chunk_offsets(sh.S, sh.P)
+    edges = sorted({o + d for o in off for d in (-1, 0, 1, 127, 128) if 0 <= o + d < sh.S})
+    rows = [(0, h, s) for h, s in zip([2, 9, 16, 21] * 12, edges[:48])]
+    o_ref, l_ref = oracle.fwd_rows(q, k, v, rows, causal=True)
+    check("out rows", torch.stack([out[b, s, h].cpu() for b, h, s in rows]), o_ref)
+    assert max(abs(lse[b, h, s].item() - l_ref[i].item()) for i, (b, h, s) in enumerate(rows)) < LSE_TOL
+    check("dq rows", torch.stack([dq[b, s, h].cpu() for b, h, s in rows[:24]]),
+          oracle.dq_rows(q, k, v, do, rows[:24], causal=True))
+    krows = [(0, 5, s) for s in edges[:16]]
+    dk_ref, dv_ref = oracle.dkv_rows(q, k, v, do, krows, causal=True)
+    check("dk rows", torch.stack([dk[b, s, h].cpu() for b, h, s in krows]), dk_ref)
+    check("dv rows", torch.stack([dv[b, s, h].cpu() for b, h, s in krows]), dv_ref)
+    dv_sum = dv.float().sum(dim=1)
+    do_sum = do.float().sum(dim=1).to(dv_sum.device)
+    assert ((dv_sum - do_sum).norm() / do_sum.norm()).item() < 2e-2
+    assert (dk.float().sum(dim=1).abs().max() / dk.float().abs().sum(dim=1).max()).item() < 2e-2
+
+
 @pytest.mark.parametrize("P", [1, 3, 5])
 @pytest.mark.parametrize("D", [64, 128])
 def test_causal_every_p_gqa(P, D):
