@@ -224,3 +224,24 @@ def test_binding_checks_element_types_before_any_call(lib):
         ctx.attn_fwd(qb[0], qb[0], qb[0], 1)
     with pytest.raises(ValueError, match="16-bit"):
         ctx.seq_head_exchange(q32, 2, 1, 0, "bshd")
+
+
+def test_plain_c_client_links_and_runs(lib, tmp_path):
+    """tests/c_client/abi_client.c includes only ctx_attn.h (as C99, with
+    warnings as errors), links the shared library and checks the host-side
+    entry points and early refusals: the boundary needs neither C++ nor
+    Python."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    libdir = os.path.dirname(ctx.library_path())
+    src = os.path.join(os.path.dirname(__file__), "c_client", "abi_client.c")
+    exe = str(tmp_path / "abi_client")
+    cmd = [gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.dirname(HEADER), src,
+           "-L", libdir, "-lctxattn", f"-Wl,-rpath,{libdir}", "-o", exe]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and "abi client ok" in r.stdout, r.stdout + r.stderr
