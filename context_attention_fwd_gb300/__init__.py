@@ -23,7 +23,7 @@ from . import build as _build
 __all__ = [
     "attn_fwd", "attn_bwd", "seq_head_exchange", "exchanged_view", "workspace_size",
     "chunk_offsets", "device_status", "selftest_wait_timeout", "library_path", "load_library",
-    "profile_enable", "profile_read",
+    "profile_enable", "profile_read", "launch_plan",
     "CtxError", "FLAG_MATERIALIZE_PARTIALS", "FLAG_KV_ALLGATHER",
 ]
 
@@ -45,6 +45,11 @@ class _Tensor(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("B", ctypes.c_int64), ("S", ctypes.c_int64),
                 ("H", ctypes.c_int64), ("D", ctypes.c_int64), ("stride_b", ctypes.c_int64),
                 ("stride_s", ctypes.c_int64), ("stride_h", ctypes.c_int64)]
+
+
+class _Plan(ctypes.Structure):
+    _fields_ = [("fwd_ctas", ctypes.c_int64), ("bwd_ctas", ctypes.c_int64), ("fwd_head_major", ctypes.c_int),
+                ("bwd_head_major", ctypes.c_int), ("bwd_group_split", ctypes.c_int)]
 
 
 def library_path() -> str:
@@ -77,11 +82,12 @@ def load_library(build_if_missing: bool = True):
             lib.ctx_selftest_exp2.argtypes = [V, V, V, ctypes.c_int64, V]
             lib.ctx_profile_enable.argtypes = [I]
             lib.ctx_profile_read.argtypes = [I, P(ctypes.c_double), P(I)]
+            lib.ctx_attn_launch_plan.argtypes = [I, I, I, I, I, I, P(I), I, P(_Plan)]
             lib.ctx_status_string.argtypes = [I]
             lib.ctx_status_string.restype = ctypes.c_char_p
             for n in ("ctx_attn_fwd", "ctx_attn_bwd", "ctx_seq_head_exchange", "ctx_chunk_offsets",
                       "ctx_get_device_status", "ctx_selftest_wait_timeout", "ctx_profile_enable",
-                      "ctx_profile_read", "ctx_selftest_exp2"):
+                      "ctx_profile_read", "ctx_selftest_exp2", "ctx_attn_launch_plan"):
                 getattr(lib, n).restype = I
             _lib = lib
     return _lib
@@ -160,6 +166,16 @@ def _like_layout(t: torch.Tensor, H: int) -> torch.Tensor:
     if t.stride(0) >= t.stride(1):  # [B,S,H,D] storage
         return torch.empty(B, S, H, D, dtype=torch.bfloat16, device=t.device)
     return torch.empty(S, B, H, D, dtype=torch.bfloat16, device=t.device).permute(1, 0, 2, 3)
+
+
+def launch_plan(B, S, Hq, Hkv, D, P, chunk_offsets=None, causal=False) -> dict:
+    """How the attention calls of these sizes will be launched (host only):
+    CTA counts, launch order (heads first or not) and the D=256 backward's
+    GQA group split."""
+    plan = _Plan()
+    _check(load_library().ctx_attn_launch_plan(B, S, Hq, Hkv, D, P, _offsets(P, chunk_offsets), int(causal),
+                                               ctypes.byref(plan)), "ctx_attn_launch_plan")
+    return {name: getattr(plan, name) for name, _ in _Plan._fields_}
 
 
 def workspace_size(B, S, Hq, Hkv, D, P, flags=0) -> int:

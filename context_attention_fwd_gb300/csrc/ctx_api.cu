@@ -457,6 +457,21 @@ int bwd_hsplit(int64_t ntiles, int S, int B, int Hq, int Hkv, int D, int causal)
     return best;
 }
 
+// Launch decisions of one call, shared by the attention entry points and
+// ctx_attn_launch_plan.
+int64_t fwd_ctas(const ChunkTable& ct, int B, int Hq, int D) {
+    return (int64_t)(D == 256 ? ct.ntiles : ct.npairs) * Hq * B;
+}
+void bwd_plan(const ChunkTable& ct, int S, int B, int Hq, int Hkv, int D, int causal, int* hsplit,
+              int* head_major, int64_t* ctas) {
+    int hs = bwd_hsplit(ct.ntiles, S, B, Hq, Hkv, D, causal);
+    if ((int64_t)B * 2 * hs > 65535) hs = 1;  // grid limit (the backward takes B <= 32767 for D = 256)
+    const int64_t n = (int64_t)ct.ntiles * Hkv * B * (D == 256 ? 2 * hs : 1);
+    *hsplit = hs;
+    *head_major = pick_head_major(causal, n);
+    if (ctas) *ctas = n;
+}
+
 size_t bwd_ws_bytes(int B, int S, int Hq, int Hkv, int D, int P) {
     const size_t slots = (size_t)B * Hq * ntiles_upper(S, P) * kTile;
     const int hs = bwd_hsplit_cap(S, B, Hq, Hkv, D);
@@ -501,6 +516,21 @@ size_t ctx_attn_workspace_size(int B, int S, int Hq, int Hkv, int D, int P, int 
     const size_t f = fwd_ws_bytes(B, S, Hq, D, P, flags);
     const size_t b = bwd_ws_bytes(B, S, Hq, Hkv, D, P);
     return f > b ? f : b;
+}
+
+int ctx_attn_launch_plan(int B, int S, int Hq, int Hkv, int D, int P, const int* chunk_offsets, int causal,
+                         ctx_launch_plan_t* plan) {
+    if (!plan || !sizes_ok(B, S, Hq, Hkv, D)) return CTX_ERR_INVALID_ARG;
+    if (D != 64 && D != 128 && D != 256) return CTX_ERR_UNSUPPORTED;
+    ChunkTable ct;
+    memset(&ct, 0, sizeof(ct));
+    const int rc = build_chunks(S, P, chunk_offsets, &ct);
+    if (rc) return rc;
+    const int c = causal ? 1 : 0;
+    plan->fwd_ctas = fwd_ctas(ct, B, Hq, D);
+    plan->fwd_head_major = pick_head_major(c, plan->fwd_ctas);
+    bwd_plan(ct, S, B, Hq, Hkv, D, c, &plan->bwd_group_split, &plan->bwd_head_major, &plan->bwd_ctas);
+    return CTX_OK;
 }
 
 int64_t ctx_exchange_padded_len(int64_t S, int ring, int ulysses) {
@@ -549,7 +579,7 @@ int ctx_attn_fwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
     p.group = (int)(Hq / Hkv);
     p.causal = causal ? 1 : 0;
     p.allgather = (flags & CTX_FLAG_KV_ALLGATHER) ? 1 : 0;
-    p.head_major = pick_head_major(p.causal, (int64_t)(D == 256 ? p.ct.ntiles : p.ct.npairs) * Hq * B);
+    p.head_major = pick_head_major(p.causal, fwd_ctas(p.ct, (int)B, (int)Hq, (int)D));
     p.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
     p.scale_log2 = p.scale * 1.4426950408889634f;
     p.out = static_cast<__nv_bfloat16*>(do_.data);
@@ -610,8 +640,8 @@ int ctx_attn_bwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
     float* lse2_t = reinterpret_cast<float*>(ws);
     float* delta_t = reinterpret_cast<float*>(ws + align256(slots * 4));
     float* dq_acc = reinterpret_cast<float*>(ws + 2 * align256(slots * 4));
-    p.hsplit = bwd_hsplit(p.ct.ntiles, (int)S, (int)B, (int)Hq, (int)Hkv, (int)D, causal);
-    if ((int64_t)B * 2 * p.hsplit > 65535) p.hsplit = 1;  // grid z limit (B <= 32767 checked above)
+    bwd_plan(p.ct, (int)S, (int)B, (int)Hq, (int)Hkv, (int)D, causal ? 1 : 0, &p.hsplit, &p.head_major,
+             nullptr);
     p.dkv_part = p.hsplit > 1 ? reinterpret_cast<float*>(ws + 2 * align256(slots * 4) + align256(slots * D * 4))
                               : nullptr;
     if (!make_tmap_bshd(&p.tq, tq.data, B, S, Hq, D, tq.sb, tq.ss, tq.sh, 64, kTile) ||
@@ -622,7 +652,6 @@ int ctx_attn_bwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
     p.B = (int)B; p.S = (int)S; p.Hq = (int)Hq; p.Hkv = (int)Hkv;
     p.group = (int)(Hq / Hkv);
     p.causal = causal ? 1 : 0;
-    p.head_major = pick_head_major(p.causal, (int64_t)p.ct.ntiles * Hkv * B * (D == 256 ? 2 * p.hsplit : 1));
     p.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
     p.scale_log2 = p.scale * 1.4426950408889634f;
     p.lse2 = lse2_t;

@@ -155,6 +155,26 @@ int ctx_attn_bwd_noalloc(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx
                          const ctx_tensor_t* dq, const ctx_tensor_t* dk, const ctx_tensor_t* dv,
                          ctx_stream_t stream);
 
+/* How the attention calls of these sizes will be launched (host only, no
+ * GPU needed; on a machine without one the SM count is taken as 148).
+ *  fwd_ctas, bwd_ctas: CTAs of the forward and backward attention kernels.
+ *  fwd_head_major, bwd_head_major: 1 when the grid is launched heads first
+ *    (tile 0 of every head before tile 1 of any), which the library does for
+ *    causal calls on grids of at most four CTAs per SM, so that the tiles
+ *    with the most causal work start first; 0 when each head's tiles are
+ *    launched together.
+ *  bwd_group_split: for D = 256, the number of CTAs over which the query
+ *    heads of one GQA group are split (1 = no split); always 1 otherwise.
+ * Returns CTX_ERR_INVALID_ARG / CTX_ERR_UNSUPPORTED for sizes the attention
+ * calls would refuse. */
+typedef struct {
+    int64_t fwd_ctas, bwd_ctas;
+    int fwd_head_major, bwd_head_major;
+    int bwd_group_split;
+} ctx_launch_plan_t;
+int ctx_attn_launch_plan(int B, int S, int Hq, int Hkv, int D, int P, const int* chunk_offsets, int causal,
+                         ctx_launch_plan_t* plan);
+
 /* Padded sequence length of the exchange: W * ceil(S / W), W = ring * ulysses. */
 int64_t ctx_exchange_padded_len(int64_t S, int ring, int ulysses);
 

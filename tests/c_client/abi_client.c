@@ -33,6 +33,12 @@ int main(void) {
     CHECK(ctx_exchange_padded_len(1001, 2, 2) == 1004);
     CHECK(ctx_exchange_padded_len(65536, 4, 2) == 65536);
 
+    /* launch plan of the 24/4-head D=256 causal model at 1024 tokens */
+    ctx_launch_plan_t plan;
+    CHECK(ctx_attn_launch_plan(1, 1024, 24, 4, 256, 2, NULL, 1, &plan) == CTX_OK);
+    CHECK(plan.fwd_ctas == 8 * 24 && plan.fwd_head_major == 1 && plan.bwd_group_split >= 1);
+    CHECK(ctx_attn_launch_plan(1, 1024, 24, 4, 96, 2, NULL, 1, &plan) == CTX_ERR_UNSUPPORTED);
+
     const char* s = ctx_status_string(CTX_ERR_TIMEOUT);
     CHECK(s != NULL && strlen(s) > 0);
 

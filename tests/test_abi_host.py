@@ -245,3 +245,52 @@ def test_plain_c_client_links_and_runs(lib, tmp_path):
     assert r.returncode == 0, r.stderr
     r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0 and "abi client ok" in r.stdout, r.stdout + r.stderr
+
+
+def test_launch_plan(lib):
+    """Launch decisions, on the host.  Without a GPU the library takes 148
+    SMs."""
+    # not causal: each head's tiles together, no group split
+    p = ctx.launch_plan(1, 32760, 24, 24, 128, 8)
+    assert (p["fwd_head_major"], p["bwd_head_major"], p["bwd_group_split"]) == (0, 0, 1)
+    assert p["fwd_ctas"] == 8 * 16 * 24 and p["bwd_ctas"] == 8 * 32 * 24  # 16 tile pairs, 32 tiles per chunk
+    # causal on a grid of many waves: still tile-major
+    p = ctx.launch_plan(1, 32760, 24, 24, 128, 8, causal=True)
+    assert (p["fwd_head_major"], p["bwd_head_major"]) == (0, 0)
+    # causal on a small grid: heads first
+    p = ctx.launch_plan(1, 777, 4, 2, 128, 3, causal=True)
+    assert (p["fwd_head_major"], p["bwd_head_major"], p["bwd_group_split"]) == (1, 1, 1)
+    # the 24/4-head D=256 causal model at 1024 tokens: heads first, group split in three
+    p = ctx.launch_plan(1, 1024, 24, 4, 256, 2, causal=True)
+    assert (p["fwd_head_major"], p["bwd_head_major"], p["bwd_group_split"]) == (1, 1, 3)
+    assert p["fwd_ctas"] == 8 * 24 and p["bwd_ctas"] == 8 * 4 * 2 * 3
+    # the same heads not causal: split in two, one wave
+    p = ctx.launch_plan(1, 1024, 24, 4, 256, 2)
+    assert (p["bwd_group_split"], p["bwd_head_major"], p["bwd_ctas"]) == (2, 0, 128)
+    # refusals as in the attention calls
+    with pytest.raises(ctx.CtxError) as e:
+        ctx.launch_plan(1, 1024, 24, 4, 96, 2)
+    assert e.value.code == 2
+    with pytest.raises(ctx.CtxError) as e:
+        ctx.launch_plan(1, 3, 1, 1, 64, 4)
+    assert e.value.code == 1
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_group_split_fits_the_workspace(lib, causal):
+    """Whatever split the backward picks, its fp32 partial rows fit in the
+    workspace that ctx_attn_workspace_size reports (any chunking of S)."""
+    import random
+    rng = random.Random(5 + causal)
+    for _ in range(40):
+        B, Hkv = rng.choice([1, 2]), rng.choice([1, 2, 4])
+        Hq = Hkv * rng.choice([1, 2, 3, 4, 6, 8])
+        S = rng.randint(1, 5000)
+        P = rng.randint(1, min(S, 16))
+        p = ctx.launch_plan(B, S, Hq, Hkv, 256, P, causal=causal)
+        ntiles_max = sum(-(-(S // P + (c < S % P)) // 128) for c in range(P))
+        need = 2 * B * Hq * ntiles_max * 128 * 4 + B * Hq * ntiles_max * 128 * 256 * 4
+        if p["bwd_group_split"] > 1:
+            need += p["bwd_group_split"] * B * Hkv * S * 2 * 256 * 4
+        assert lib.ctx_attn_workspace_size(B, S, Hq, Hkv, 256, P, 0) >= need
+        assert (Hq // Hkv) % p["bwd_group_split"] == 0
