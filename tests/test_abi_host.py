@@ -294,3 +294,15 @@ def test_group_split_fits_the_workspace(lib, causal):
             need += p["bwd_group_split"] * B * Hkv * S * 2 * 256 * 4
         assert lib.ctx_attn_workspace_size(B, S, Hq, Hkv, 256, P, 0) >= need
         assert (Hq // Hkv) % p["bwd_group_split"] == 0
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_launch_order_rule(lib, D):
+    """Heads first exactly for causal calls on grids of at most four CTAs per
+    SM (148 SMs without a GPU), for both kernels."""
+    for S in (64, 500, 1024, 3000, 8192, 20000):
+        for Hq, Hkv in ((24, 24), (24, 4), (4, 2)):
+            for causal in (False, True):
+                p = ctx.launch_plan(1, S, Hq, Hkv, D, 4, causal=causal)
+                assert p["fwd_head_major"] == int(causal and p["fwd_ctas"] <= 4 * 148)
+                assert p["bwd_head_major"] == int(causal and p["bwd_ctas"] <= 4 * 148)
