@@ -5,8 +5,6 @@ Tolerance (bf16 inputs, fp32 accumulation, bf16 outputs): per tensor both
   ||got - ref||_2 / ||ref||_2 <= 2e-2   and   max|got - ref| / max|ref| <= 2e-2.
 lse (fp32 output) is held to 1e-3 absolute.
 """
-import math
-
 import pytest
 import torch
 
