@@ -66,3 +66,8 @@ def test_reference_arm_under_torchrun_two_ranks():
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
     assert rec["cpu_baseline"]["kind"] == "oracle" and rec["e2e"]["h2d_bytes_per_step"] == 0
+    contract = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"}
+    assert contract <= set(rec), contract - set(rec)
+    assert rec["steps"] == 1 and rec["warmup"] == 3 and rec["higher_is_better"] is True
+    assert "workload" in rec["config"] and rec["e2e"]["value"] == rec["value"]
