@@ -46,6 +46,11 @@ NCU_BWD = {"bytes_per_launch": 1333379584 + 891769088,  # dram read + write, S=3
            "source_sha256": "3baf3598575a13e3ca1baa4313d321326d8e59a4ef8a88d7326c10300336c076"}
 
 
+# Dense bf16 tensor-core rate of one SM per clock: one M=128, N=128, K=16
+# tcgen05 product (2 flop per multiply-add) every 64 clocks.
+TC_FLOP_PER_CLK_SM = 128 * 128 * 16 * 2 // 64
+
+
 def flops_fwd(sh: AttnShape) -> float:
     return 4.0 * sh.B * sh.Hq * sh.S * sh.S * sh.D
 
@@ -119,6 +124,34 @@ class ClockSampler:
         os.unlink(self.path)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def tensor_peaks(peaks, clocks, n_sm):
+    """The denominators of the tensor-core roofline for a kernel timed under
+    `clocks` (the nvidia-smi samples of the timed region):
+      measured -- the cuBLAS bf16 GEMM of MEASURED_PEAKS.json: the burst figure
+                  when the SM clock's median sat at its maximum (no power or
+                  thermal cap held it down), else the sustained one;
+      clock    -- the tensor cores' own rate at the sampled median SM clock:
+                  SMs x MHz x TC_FLOP_PER_CLK_SM."""
+    mhz, mx = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    at_max = bool(mhz and mx and mhz >= 0.97 * mx)
+    measured = peaks["bf16"] if at_max else peaks["bf16_sustained"]
+    kind = (f"bf16 dense, {'burst' if at_max else 'sustained'} ({peaks['source']}): "
+            f"SM clock median {mhz} of {mx} MHz in the timed region")
+    clock = n_sm * mhz * 1e6 * TC_FLOP_PER_CLK_SM / 1e12 if mhz else None
+    return measured, kind, clock
+
+
+def roofline_entry(kernel, achieved, peaks, clocks, n_sm, **extra):
+    measured, kind, clock = tensor_peaks(peaks, clocks, n_sm)
+    d = {"kernel": kernel, "bound": "tensor", "achieved": achieved, "peak": measured, "unit": "TFLOP/s",
+         "frac": achieved / measured, "peak_kind": kind,
+         "frac_burst": achieved / peaks["bf16"], "frac_sustained": achieved / peaks["bf16_sustained"],
+         "clock_peak": clock, "frac_clock_peak": achieved / clock if clock else None,
+         "sm_mhz": clocks.get("sm_mhz")}
+    d.update(extra)
+    return d
 
 
 def dist_setup():
@@ -549,8 +582,9 @@ def main():
                if not args.shape and NCU_BWD["source_sha256"] == source_sha(bwd_src) else None)
     kname = "attn_fwd256_kernel" if sh.D == 256 else f"attn_fwd_kernel<{sh.D}>"
     bname = "attn_bwd256_kernel" if sh.D == 256 else f"attn_bwd_kernel<{sh.D}>"
-    peak = peaks["bf16_sustained"]
     clocks = clk.summary()
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    _, _, clock_peak = tensor_peaks(peaks, clocks, n_sm)
 
     # ------------------------------------------------ end to end, host buffers
     e2e = None
@@ -587,16 +621,16 @@ def main():
         "config": config_dict(),
         "pct_of_peak": {"burst": 100.0 * value / world / peaks["bf16"],
                         "sustained": 100.0 * value / world / peaks["bf16_sustained"],
-                        "peaks_source": peaks["source"]},
+                        "clock_derived": (100.0 * value / world / clock_peak) if clock_peak else None,
+                        "clock_derived_tflops": clock_peak,
+                        "peaks_source": peaks["source"],
+                        "note": "burst / sustained: the measured cuBLAS bf16 GEMM; clock_derived: "
+                                f"{n_sm} SMs x median SM MHz x {TC_FLOP_PER_CLK_SM} flop/clk/SM"},
         "clocks": clocks,
         "gpu_launches": 4 * args.steps,
-        "roofline": {"kernel": bname, "bound": "tensor", "achieved": bwd_tf,
-                     "peak": peak, "unit": "TFLOP/s", "frac": bwd_tf / peak, "traffic": traffic,
-                     "peak_kind": f"bf16 dense, sustained ({peaks['source']})",
-                     "launches": bwd_n, "avg_ms": bwd_avg},
-        "roofline_fwd": {"kernel": kname, "bound": "tensor", "achieved": fwd_tf,
-                         "peak": peak, "unit": "TFLOP/s", "frac": fwd_tf / peak,
-                         "launches": fwd_n, "avg_ms": fwd_avg},
+        "roofline": roofline_entry(bname, bwd_tf, peaks, clocks, n_sm, traffic=traffic,
+                                   launches=bwd_n, avg_ms=bwd_avg),
+        "roofline_fwd": roofline_entry(kname, fwd_tf, peaks, clocks, n_sm, launches=fwd_n, avg_ms=fwd_avg),
         "exchange": exchange,
         "d256": d256,
         "causal": causal,

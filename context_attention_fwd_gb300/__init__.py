@@ -23,12 +23,13 @@ from . import build as _build
 __all__ = [
     "attn_fwd", "attn_bwd", "seq_head_exchange", "exchanged_view", "workspace_size",
     "chunk_offsets", "device_status", "selftest_wait_timeout", "library_path", "load_library",
-    "profile_enable", "profile_read", "launch_plan",
-    "CtxError", "FLAG_MATERIALIZE_PARTIALS", "FLAG_KV_ALLGATHER",
+    "profile_enable", "profile_read", "launch_plan", "debug_set", "kernel_binary_version",
+    "CtxError", "FLAG_MATERIALIZE_PARTIALS", "FLAG_KV_ALLGATHER", "DEBUG_SKIP_ARRIVAL",
 ]
 
 FLAG_MATERIALIZE_PARTIALS = 1
 FLAG_KV_ALLGATHER = 2
+DEBUG_SKIP_ARRIVAL = 1
 LAYOUT_BSHD, LAYOUT_SBHD = 0, 1
 _lock = threading.Lock()
 _lib = None
@@ -83,11 +84,14 @@ def load_library(build_if_missing: bool = True):
             lib.ctx_profile_enable.argtypes = [I]
             lib.ctx_profile_read.argtypes = [I, P(ctypes.c_double), P(I)]
             lib.ctx_attn_launch_plan.argtypes = [I, I, I, I, I, I, P(I), I, P(_Plan)]
+            lib.ctx_debug_set.argtypes = [ctypes.c_uint, ctypes.c_uint]
+            lib.ctx_kernel_binary_version.argtypes = [P(I)]
             lib.ctx_status_string.argtypes = [I]
             lib.ctx_status_string.restype = ctypes.c_char_p
             for n in ("ctx_attn_fwd", "ctx_attn_bwd", "ctx_seq_head_exchange", "ctx_chunk_offsets",
                       "ctx_get_device_status", "ctx_selftest_wait_timeout", "ctx_profile_enable",
-                      "ctx_profile_read", "ctx_selftest_exp2", "ctx_attn_launch_plan"):
+                      "ctx_profile_read", "ctx_selftest_exp2", "ctx_attn_launch_plan", "ctx_debug_set",
+                      "ctx_kernel_binary_version"):
                 getattr(lib, n).restype = I
             _lib = lib
     return _lib
@@ -326,3 +330,18 @@ def selftest_wait_timeout(timeout_us: int = 20000):
     s = torch.cuda.current_stream().cuda_stream
     _check(load_library().ctx_selftest_wait_timeout(timeout_us, ctypes.c_void_p(s)),
            "ctx_selftest_wait_timeout")
+
+
+def debug_set(flags: int = 0, wait_limit_ms: int = 0):
+    """Test-only switches of the library (``ctx_debug_set``): DEBUG_SKIP_ARRIVAL
+    makes every attention kernel's producer leave out one load step so that a
+    bounded device wait runs out; wait_limit_ms overrides the wait limit
+    (0 = default).  ``debug_set()`` restores normal operation."""
+    _check(load_library().ctx_debug_set(flags, wait_limit_ms), "ctx_debug_set")
+
+
+def kernel_binary_version() -> int:
+    """cudaFuncAttributes.binaryVersion of the attention kernels on the current device (103 = sm_103a)."""
+    v = ctypes.c_int()
+    _check(load_library().ctx_kernel_binary_version(ctypes.byref(v)), "ctx_kernel_binary_version")
+    return v.value

@@ -174,7 +174,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             QTileIter q = q0;
             int last_ph[2] = {-1, -1};
             bool ok = true;
+            const int skip = debug_skip_step(p.debug, n_q);  // -1 in normal use
             for (int i = 0; i < n_q; ++i, next(q)) {
+                if (i == skip) continue;  // failure injection: Q_i, dO_i never arrive
                 const int st = i & 1, ph = (i >> 1) & 1;
                 if (!(ok = mbar_wait(smem_u32(&bars.q_empty[st]), ph ^ 1, wc))) break;
                 const uint32_t qf = smem_u32(&bars.q_full[st]);
@@ -456,8 +458,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
 template <int D, bool kHeadMajor>
 int launch_bwd_do(const BwdParams& p, cudaStream_t s) {
     using L = BwdLayout<D>;
-    if (cudaFuncSetAttribute(attn_bwd_kernel<D, kHeadMajor>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::SMEM) != cudaSuccess)
+    static OncePerDevice attr;
+    if (!attr.run([] {
+            return cudaFuncSetAttribute(attn_bwd_kernel<D, kHeadMajor>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        L::SMEM) == cudaSuccess;
+        }))
         return 4;
     attn_bwd_kernel<D, kHeadMajor><<<grid_dims(kHeadMajor, p.ct.ntiles, p.Hkv, p.B), kThreads, L::SMEM, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;

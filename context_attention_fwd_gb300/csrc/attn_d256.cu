@@ -134,9 +134,11 @@ __global__ void __launch_bounds__(kF256Threads, 1) attn_fwd256_kernel(const __gr
             int last[L::SLOTS];
             for (int i = 0; i < L::SLOTS; ++i) last[i] = -1;
             bool ok = true;
+            const int skip = debug_skip_step(p.debug, n_kv);  // -1 in normal use
             KvWalk w;
             kv_first(ct, g, w);
             for (int j = 0; j < n_kv && ok; ++j, kv_next(ct, g, w)) {
+                if (j == skip) continue;  // failure injection: K(j), V(j) never arrive
                 const int kv_start = ct.off[w.c] + (w.t - w.t0) * kTile;
                 for (int k = 0; k < L::LOADS; ++k) {
                     const int n = j * L::LOADS + k, slot = n % L::SLOTS, ph = (n / L::SLOTS) & 1;
@@ -493,7 +495,9 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
             QTileIter q = q0;
             int last[L::SLOTS] = {-1, -1, -1, -1};
             bool ok = true;
+            const int skip = debug_skip_step(p.debug, n_q);  // -1 in normal use
             for (int i = 0; i < n_q && ok; ++i, qw.next(q)) {
+                if (i == skip) continue;  // failure injection: query tile i's loads never arrive
                 const int q_start = qw.first_row(q);
                 for (int k = 0; k < L::LOADS; ++k) {
                     const int n = i * L::LOADS + k;
@@ -798,7 +802,10 @@ int launch_attn_fwd256(const FwdParams& p, cudaStream_t s) {
     const bool partials = p.part_o != nullptr;
     auto kern = partials ? (p.head_major ? attn_fwd256_kernel<true, true> : attn_fwd256_kernel<true, false>)
                          : (p.head_major ? attn_fwd256_kernel<false, true> : attn_fwd256_kernel<false, false>);
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, F256::SMEM) != cudaSuccess)
+    static OncePerDevice attr[4];
+    if (!attr[(partials ? 2 : 0) + (p.head_major ? 1 : 0)].run([&] {
+            return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, F256::SMEM) == cudaSuccess;
+        }))
         return 4;
     kern<<<grid_dims(p.head_major, p.ct.ntiles, p.Hq, p.B), kF256Threads, F256::SMEM, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
@@ -806,7 +813,10 @@ int launch_attn_fwd256(const FwdParams& p, cudaStream_t s) {
 
 int launch_attn_bwd256(const BwdParams& p, cudaStream_t s) {
     auto kern = p.head_major ? attn_bwd256_kernel<true> : attn_bwd256_kernel<false>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, B256::SMEM) != cudaSuccess)
+    static OncePerDevice attr[2];
+    if (!attr[p.head_major ? 1 : 0].run([&] {
+            return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, B256::SMEM) == cudaSuccess;
+        }))
         return 4;
     // z = 2 (b * hsplit + split) + column half
     kern<<<grid_dims(p.head_major, p.ct.ntiles, p.Hkv, p.B * 2 * p.hsplit), kB256Threads, B256::SMEM, s>>>(p);

@@ -153,9 +153,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     tma_tile(p.tq, sQ + x * L::TILE + bx * L::BOX, qf, bx * 64, qs0 + x * kTile, h, b);
             int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
             bool ok = true;
+            const int skip = debug_skip_step(p.debug, n_kv);  // -1 in normal use
             KvWalk w;
             kv_first(ct, g, w);
             for (int j = 0; j < n_kv; ++j, kv_next(ct, g, w)) {
+                if (j == skip) continue;  // failure injection: K(j), V(j) never arrive
                 const int st = j & 1, ph = (j >> 1) & 1;
                 const int kv_start = ct.off[w.c] + (w.t - w.t0) * kTile;
                 if (!(ok = mbar_wait(smem_u32(&bars.k_empty[st]), ph ^ 1, wc))) break;
@@ -395,8 +397,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 template <int D, bool kPartials, bool kHeadMajor>
 int launch_fwd_dpo(const FwdParams& p, cudaStream_t s) {
     using L = FwdLayout<D>;
-    if (cudaFuncSetAttribute(attn_fwd_kernel<D, kPartials, kHeadMajor>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::SMEM) != cudaSuccess)
+    static OncePerDevice attr;
+    if (!attr.run([] {
+            return cudaFuncSetAttribute(attn_fwd_kernel<D, kPartials, kHeadMajor>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) == cudaSuccess;
+        }))
         return 4;
     attn_fwd_kernel<D, kPartials, kHeadMajor>
         <<<grid_dims(kHeadMajor, p.ct.npairs, p.Hq, p.B), kThreads, L::SMEM, s>>>(p);
@@ -416,6 +421,12 @@ int launch_fwd_d(const FwdParams& p, cudaStream_t s) {
 }
 
 }  // namespace
+
+int attn_fwd_binary_version() {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, attn_fwd_kernel<128, false, false>) != cudaSuccess) return -1;
+    return a.binaryVersion;
+}
 
 int launch_attn_fwd(const FwdParams& p, int D, cudaStream_t s) {
     if (D == 64) return launch_fwd_d<64>(p, s);

@@ -8,9 +8,12 @@
 #include <stdlib.h>
 
 #include <algorithm>
+#include <atomic>
 #include <functional>
 #include <mutex>
 #include <vector>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/ctx_attn.h"
 #include "internal.h"
@@ -24,9 +27,11 @@ namespace {
 __device__ int g_device_status;
 
 int* status_ptr() {
+    static std::mutex mu;
     static int* ptrs[64] = {nullptr};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
     if (!ptrs[dev]) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
@@ -35,7 +40,13 @@ int* status_ptr() {
     return ptrs[dev];
 }
 
+// Test-only switches set by ctx_debug_set (0 in normal use).
+std::atomic<unsigned> g_debug_flags{0};
+std::atomic<unsigned> g_wait_limit_ms{0};  // 0: the environment's or the default limit
+
 uint64_t timeout_ns() {
+    const unsigned over = g_wait_limit_ms.load(std::memory_order_relaxed);
+    if (over) return (uint64_t)over * 1000000ull;
     static uint64_t ns = 0;
     if (!ns) {
         const char* e = getenv("CTX_ATTN_WAIT_LIMIT_MS");
@@ -44,6 +55,27 @@ uint64_t timeout_ns() {
     }
     return ns;
 }
+
+int kernel_debug_bits() {
+    return (g_debug_flags.load(std::memory_order_relaxed) & CTX_DEBUG_SKIP_ARRIVAL) ? kDebugSkipArrival : 0;
+}
+
+// CTX_ATTN_LOG=1: one line per attention call on stderr (schedule, tiles,
+// kernel variant).
+bool log_enabled() {
+    static const bool on = [] {
+        const char* e = getenv("CTX_ATTN_LOG");
+        return e && *e && *e != '0';
+    }();
+    return on;
+}
+
+// An NVTX range around an entry point (visible in a profiler's timeline;
+// nearly free when no tool is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
 
 int num_sms() {
     int dev = 0, n = 0;
@@ -388,14 +420,15 @@ size_t fwd_ws_bytes(int B, int S, int Hq, int D, int P, int flags) {
 // be split over d CTAs per (KV tile, column half), each writing fp32 partial
 // dK/dV rows that dkv_reduce_kernel sums.  The workspace holds the partial
 // rows of the largest split a call may use: the smallest divisor d of the
-// group size that brings the grid to >= 148 CTAs at the fewest tiles any
-// chunking of S has (ceil(S / 128)).
+// group size that brings the grid to at least one CTA per SM of the current
+// device at the fewest tiles any chunking of S has (ceil(S / 128)).
 int bwd_hsplit_cap(int S, int B, int Hq, int Hkv, int D) {
     if (D != 256) return 1;
     const int G = Hq / Hkv;
+    const int nsm = num_sms();
     const int64_t base = (int64_t)((S + kTile - 1) / kTile) * Hkv * 2 * B;
     for (int d = 1; d < G; ++d)
-        if (G % d == 0 && base * d >= 148) return d;
+        if (G % d == 0 && base * d >= nsm) return d;
     return G;
 }
 
@@ -543,6 +576,7 @@ int ctx_attn_fwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
                  const int* chunk_offsets, ctx_layout_t layout, int causal, float scale,
                  const ctx_tensor_t* out, float* lse, void* workspace, size_t workspace_bytes,
                  int flags, ctx_stream_t stream) {
+    NvtxRange range("ctx_attn_fwd");
     if (!q || !k || !v || !out || !lse) return CTX_ERR_INVALID_ARG;
     if (layout != CTX_LAYOUT_BSHD && layout != CTX_LAYOUT_SBHD) return CTX_ERR_INVALID_ARG;
     if (flags & ~(CTX_FLAG_MATERIALIZE_PARTIALS | CTX_FLAG_KV_ALLGATHER)) return CTX_ERR_INVALID_ARG;
@@ -587,8 +621,17 @@ int ctx_attn_fwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
     p.lse = lse;
     p.status = status_ptr();
     p.timeout_ns = timeout_ns();
+    p.debug = kernel_debug_bits();
     if (!p.status) return CTX_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (log_enabled())
+        fprintf(stderr,
+                "ctx_attn_fwd: B=%d S=%d Hq=%d Hkv=%d D=%d P=%d causal=%d order=%s partials=%d | %d query "
+                "tiles, %lld CTAs (%s), grid order %s\n",
+                p.B, p.S, p.Hq, p.Hkv, (int)D, P, p.causal, p.allgather ? "all-gather" : "ring", partials ? 1 : 0,
+                p.ct.ntiles, (long long)fwd_ctas(p.ct, p.B, p.Hq, (int)D),
+                D == 256 ? "attn_fwd256_kernel, one tile per CTA" : "attn_fwd_kernel, two tiles per CTA",
+                p.head_major ? "head-major" : "tile-major");
     prof_record(0, 0, s);
     rc = launch_attn_fwd(p, (int)D, s);
     prof_record(0, 1, s);
@@ -609,6 +652,7 @@ int ctx_attn_bwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
                  const int* chunk_offsets, ctx_layout_t layout, int causal, float scale,
                  const ctx_tensor_t* dq, const ctx_tensor_t* dk, const ctx_tensor_t* dv,
                  void* workspace, size_t workspace_bytes, ctx_stream_t stream) {
+    NvtxRange range("ctx_attn_bwd");
     if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv) return CTX_ERR_INVALID_ARG;
     if (layout != CTX_LAYOUT_BSHD && layout != CTX_LAYOUT_SBHD) return CTX_ERR_INVALID_ARG;
     const int64_t B = q->B, S = q->S, Hq = q->H, D = q->D, Hkv = k->H;
@@ -640,8 +684,9 @@ int ctx_attn_bwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
     float* lse2_t = reinterpret_cast<float*>(ws);
     float* delta_t = reinterpret_cast<float*>(ws + align256(slots * 4));
     float* dq_acc = reinterpret_cast<float*>(ws + 2 * align256(slots * 4));
+    int64_t bwd_ctas = 0;
     bwd_plan(p.ct, (int)S, (int)B, (int)Hq, (int)Hkv, (int)D, causal ? 1 : 0, &p.hsplit, &p.head_major,
-             nullptr);
+             &bwd_ctas);
     p.dkv_part = p.hsplit > 1 ? reinterpret_cast<float*>(ws + 2 * align256(slots * 4) + align256(slots * D * 4))
                               : nullptr;
     if (!make_tmap_bshd(&p.tq, tq.data, B, S, Hq, D, tq.sb, tq.ss, tq.sh, 64, kTile) ||
@@ -662,8 +707,16 @@ int ctx_attn_bwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
     p.k_sb = tdk.sb; p.k_ss = tdk.ss; p.k_sh = tdk.sh;
     p.status = status_ptr();
     p.timeout_ns = timeout_ns();
+    p.debug = kernel_debug_bits();
     if (!p.status) return CTX_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (log_enabled())
+        fprintf(stderr,
+                "ctx_attn_bwd: B=%d S=%d Hq=%d Hkv=%d D=%d P=%d causal=%d | %d KV tiles, %lld CTAs (%s), "
+                "GQA group split %d, grid order %s\n",
+                p.B, p.S, p.Hq, p.Hkv, (int)D, P, p.causal, p.ct.ntiles, (long long)bwd_ctas,
+                D == 256 ? "attn_bwd256_kernel, column halves" : "attn_bwd_kernel, one KV tile per CTA",
+                p.hsplit, p.head_major ? "head-major" : "tile-major");
     if (cudaMemsetAsync(dq_acc, 0, slots * D * 4, s) != cudaSuccess) return CTX_ERR_CUDA;
     {
         const int64_t threads = (int64_t)slots * (D / 8);
@@ -743,6 +796,7 @@ int ctx_attn_bwd_noalloc(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx
 
 int ctx_seq_head_exchange(const ctx_tensor_t* x, void* y, int ring, int ulysses, int dir,
                           ctx_layout_t layout, ctx_stream_t stream) {
+    NvtxRange range("ctx_seq_head_exchange");
     if (!x || !x->data || !y || ring < 1 || ulysses < 1 || (dir != 0 && dir != 1))
         return CTX_ERR_INVALID_ARG;
     if (layout != CTX_LAYOUT_BSHD && layout != CTX_LAYOUT_SBHD) return CTX_ERR_INVALID_ARG;
@@ -805,6 +859,22 @@ int ctx_selftest_exp2(const float* x, float* y_poly, float* y_sfu, int64_t n, ct
     exp2_selftest_kernel<<<(unsigned)((n + 255) / 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         x, y_poly, y_sfu, n);
     return launch_status();
+}
+
+int ctx_debug_set(unsigned flags, unsigned wait_limit_ms) {
+    if (flags & ~(unsigned)CTX_DEBUG_SKIP_ARRIVAL) return CTX_ERR_INVALID_ARG;
+    if (wait_limit_ms > 60u * 1000u) return CTX_ERR_INVALID_ARG;
+    g_wait_limit_ms.store(wait_limit_ms, std::memory_order_relaxed);
+    g_debug_flags.store(flags, std::memory_order_relaxed);
+    return CTX_OK;
+}
+
+int ctx_kernel_binary_version(int* version) {
+    if (!version) return CTX_ERR_INVALID_ARG;
+    const int v = attn_fwd_binary_version();
+    if (v < 0) return CTX_ERR_CUDA;
+    *version = v;
+    return CTX_OK;
 }
 
 int ctx_selftest_wait_timeout(unsigned timeout_us, ctx_stream_t stream) {

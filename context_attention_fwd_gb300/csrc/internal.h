@@ -6,12 +6,44 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "tmap.h"
 
 namespace ctxattn {
 
 constexpr int kMaxChunks = 64;
 constexpr int kTile = 128;  // rows of a query or key/value tile
+
+// Test-only switches carried by the parameter blocks (values of the
+// CTX_DEBUG_* bits of the C ABI).  kDebugSkipArrival: the TMA producer of
+// the attention kernel leaves out the loads (and their mbarrier arrival) of
+// its second load step, so a consumer's bounded wait runs out and the
+// kernel takes its abort path.
+constexpr int kDebugSkipArrival = 1;
+
+// Index of the load step a producer leaves out under kDebugSkipArrival, or
+// -1: the second of n steps (the first when there is only one).
+__host__ __device__ inline int debug_skip_step(int debug, int n) {
+    return (debug & kDebugSkipArrival) ? (n > 1 ? 1 : 0) : -1;
+}
+
+// A set-up that is done once per device (a kernel's shared-memory limit is
+// an attribute of the function on each device; setting it on every launch
+// costs host time).  f() returns true on success.
+struct OncePerDevice {
+    std::atomic<uint64_t> done{0};
+    template <typename F>
+    bool run(F&& f) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return false;
+        const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+        if (bit && (done.load(std::memory_order_acquire) & bit)) return true;
+        if (!f()) return false;
+        if (bit) done.fetch_or(bit, std::memory_order_acq_rel);
+        return true;
+    }
+};
 
 // Ring chunk table: chunk c holds rows [off[c], off[c+1]) and 128-row tiles
 // [tile_off[c], tile_off[c+1]) of the tile numbering (tiles never straddle
@@ -49,6 +81,7 @@ struct FwdParams {
     int* status;
     uint64_t timeout_ns;
     int head_major;  // launch order of the attention kernel (grid_pos in walk.cuh)
+    int debug;       // kDebug* bits (0 in normal use)
 };
 
 struct BwdParams {
@@ -74,6 +107,7 @@ struct BwdParams {
     int* status;
     uint64_t timeout_ns;
     int head_major;  // launch order of the attention kernel (grid_pos in walk.cuh)
+    int debug;       // kDebug* bits (0 in normal use)
 };
 
 int launch_attn_fwd(const FwdParams& p, int D, cudaStream_t s);
@@ -81,5 +115,8 @@ int launch_attn_bwd(const BwdParams& p, int D, cudaStream_t s);
 // head dimension 256 (attn_d256.cu); the forward's V map uses 64-row boxes
 int launch_attn_fwd256(const FwdParams& p, cudaStream_t s);
 int launch_attn_bwd256(const BwdParams& p, cudaStream_t s);
+// cudaFuncAttributes::binaryVersion of the D = 128 forward kernel (the
+// architecture its machine code was built for, e.g. 103), or -1
+int attn_fwd_binary_version();
 
 }  // namespace ctxattn

@@ -244,8 +244,10 @@ __device__ __forceinline__ float ex2(float x) {
 // [-0.5, 0.5] whose coefficients are a Remez (minimax relative error) fit
 // computed for this library (max relative error 7.5e-5, below bf16's 3.9e-3),
 // and j added to the exponent field.  x is clamped at -125 (so the result
-// stays a normal number): very negative arguments give 2^-125 instead of 0.  Used for part of the exponentials so
-// that the SFU and the FMA pipe share the work.
+// stays a normal number): very negative arguments give 2^-125 instead of 0,
+// where ex2() gives 0.  No attention kernel calls it: sharing the
+// exponentials between the SFU and the FMA pipe was measured and was slower,
+// so only ctx_selftest_exp2 keeps it.
 __device__ __forceinline__ float ex2_poly(float x) {
     x = fmaxf(x, -125.0f);
     const float t = x + 12582912.0f;

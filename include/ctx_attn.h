@@ -22,8 +22,15 @@
  *  - Work is enqueued on the caller's stream and is asynchronous; no entry
  *    point synchronises except ctx_get_device_status.  With the workspace
  *    and outputs given, a call may be captured in a CUDA graph (after one
- *    uncaptured call with the same head dimension, which sets the kernels'
- *    shared-memory attributes).
+ *    uncaptured call with the same head dimension on that device, which sets
+ *    the kernels' shared-memory attributes once per device and looks up the
+ *    device status word).  The library caches per-device addresses of its
+ *    own device variables; they are invalid after cudaDeviceReset, so reload
+ *    the library after a reset.
+ *  - Diagnostics: CTX_ATTN_LOG=1 in the environment prints one line per
+ *    attention call to stderr (chunks, tiles, CTAs, kernel variant, launch
+ *    order); every entry point that launches work opens an NVTX range named
+ *    after it.
  *  - Arguments are validated before anything is launched; an invalid call
  *    returns an error code and writes nothing (never a silent wrong result).
  *  - Element type: bf16 for q, k, v, out, dout, dq, dk, dv; fp32 for lse.
@@ -208,10 +215,12 @@ int ctx_get_device_status(ctx_stream_t stream);
  * status word and returns.  Nothing faults or hangs. */
 int ctx_selftest_wait_timeout(unsigned timeout_us, ctx_stream_t stream);
 
-/* Self test of the exponentials inside the attention kernels: for n inputs
- * x (device fp32), writes 2^x computed by the polynomial the kernels run on
- * the FMA pipe (y_poly) and by the SFU instruction (y_sfu), so that a test can
- * hold both against a reference exp2.  Device buffers, n <= 2^31. */
+/* Self test of two exponentials: for n inputs x (device fp32), writes 2^x
+ * computed by the SFU instruction the attention kernels use (y_sfu) and by a
+ * cubic on the FMA pipe (y_poly: an alternative that was measured and not
+ * adopted; no kernel calls it, it clamps x at -125 where the SFU returns 0),
+ * so that a test can hold both against a reference exp2.  Device buffers,
+ * n <= 2^31. */
 int ctx_selftest_exp2(const float* x, float* y_poly, float* y_sfu, int64_t n, ctx_stream_t stream);
 
 /* Kernel timing for measurement.  While enabled, every launch of the
@@ -224,6 +233,28 @@ int ctx_selftest_exp2(const float* x, float* y_poly, float* y_sfu, int64_t n, ct
  * the events are created on first use. */
 int ctx_profile_enable(int enable);
 int ctx_profile_read(int kernel, double* total_ms, int* launches);
+
+/* Test-only switches (failure detection; the pages have no counterpart).
+ * ctx_debug_set(flags, wait_limit_ms) applies to the attention calls made
+ * after it, process-wide, until it is called again; ctx_debug_set(0, 0)
+ * restores normal operation.
+ *  CTX_DEBUG_SKIP_ARRIVAL: the TMA producer of every attention kernel
+ *    (forward and backward, every head dimension) leaves out the loads of its
+ *    second load step and their mbarrier arrival.  A consumer's bounded wait
+ *    then runs out; the kernel records CTX_ERR_TIMEOUT in the device status
+ *    word, waits (bounded) for its own copies and products in flight, frees
+ *    its tensor memory and returns, with its outputs incomplete.  Nothing
+ *    faults or hangs, and the next normal call computes correctly.
+ *  wait_limit_ms: the limit of every device-side wait (1 .. 60000 ms); 0 keeps
+ *    CTX_ATTN_WAIT_LIMIT_MS from the environment, else 2000 ms.
+ * CTX_ERR_INVALID_ARG for unknown flag bits or a limit above 60 s. */
+#define CTX_DEBUG_SKIP_ARRIVAL 1u
+int ctx_debug_set(unsigned flags, unsigned wait_limit_ms);
+
+/* Architecture the attention kernels' machine code was built for, as
+ * cudaFuncAttributes::binaryVersion (103 for sm_103a), on the current
+ * device.  CTX_ERR_CUDA if the kernels cannot run on it. */
+int ctx_kernel_binary_version(int* version);
 
 /* Human-readable text of a status code. */
 const char* ctx_status_string(int status);

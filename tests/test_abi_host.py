@@ -35,11 +35,20 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_library_is_built_for_sm103a():
-    so = ctx.library_path()
-    assert os.path.exists(so)
-    # the fatbinary names the architecture it carries; no other SASS is embedded
-    data = open(so, "rb").read()
-    assert b"sm_103a" in data
+    """The build compiles every translation unit and links for sm_103a
+    only (one -gencode, no PTX for other targets), and the library on disk
+    is up to date with the sources.  On a GPU the runtime's binaryVersion
+    of the kernels is checked too (tests/test_failure_gpu.py)."""
+    from context_attention_fwd_gb300 import build as b
+    assert b.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert os.path.exists(ctx.library_path()) and b.up_to_date()
+
+
+def test_debug_switches_validate_their_arguments(lib):
+    assert lib.ctx_debug_set(0x80, 0) == 1       # unknown flag bit
+    assert lib.ctx_debug_set(0, 60001) == 1      # wait limit above 60 s
+    assert lib.ctx_debug_set(1, 100) == 0
+    assert lib.ctx_debug_set(0, 0) == 0          # back to normal operation
 
 
 @pytest.mark.parametrize("S,P", [(1001, 4), (32760, 8), (512, 2), (4608, 4), (5, 5), (17, 3), (65536, 4)])

@@ -103,10 +103,10 @@ def test_gqa_group_split(B, S, Hq, Hkv, P):
 
 def test_long_context_s16384_causal_sampled():
     """The same heads at 16384 tokens, P=8, causal, as the bench times them:
-    sampled query rows (out, lse, dq) at chunk and tile edges against the
-    oracle, and the sum rules for dk and dv over each key/value head's
-    group (the oracle's key-row gradients need every row's statistics,
-    too slow here at this size; the key-row path is checked at 1024 tokens)."""
+    sampled query rows (out, lse, dq) and key rows of one key/value head
+    (dk, dv: every query row of its six-head group enters them) at chunk and
+    tile edges against the oracle, plus the sum rules for dk and dv over
+    every key/value head's group."""
     sh = AttnShape(B=1, S=16384, Hq=24, Hkv=4, D=256, P=8)
     inputs, outputs = run_gpu(sh, causal=True)
     q, k, v, do = inputs
@@ -119,6 +119,11 @@ def test_long_context_s16384_causal_sampled():
     assert max(abs(lse[b, h, s].item() - l_ref[i].item()) for i, (b, h, s) in enumerate(rows)) < LSE_TOL
     check("dq rows", torch.stack([dq[b, s, h].cpu() for b, h, s in rows[:24]]),
           oracle.dq_rows(q, k, v, do, rows[:24], causal=True))
+    # key rows at chunk and tile edges, the sequence's first and last rows
+    krows = [(0, 2, s) for s in sorted(set(edges[:14]) | {sh.S - 1})]
+    dk_ref, dv_ref = oracle.dkv_rows(q, k, v, do, krows, causal=True)
+    check("dk rows", torch.stack([dk[b, s, h].cpu() for b, h, s in krows]), dk_ref)
+    check("dv rows", torch.stack([dv[b, s, h].cpu() for b, h, s in krows]), dv_ref)
     G = sh.Hq // sh.Hkv
     dv_sum = dv.float().sum(dim=1)  # [B, Hkv, D]
     do_sum = do.float().sum(dim=1).view(sh.B, sh.Hkv, G, sh.D).sum(dim=2).to(dv_sum.device)

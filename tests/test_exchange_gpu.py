@@ -125,7 +125,9 @@ def test_hybrid_ring4_ulysses2_full_size_sampled():
     """The ring 4 x ulysses 2 hybrid at full size: exchange of
     [1,65536,32,128] (k, v with 8 heads), GQA 32/8 attention over 4 ring
     chunks on the exchanged tensors, inverse exchange; forward and backward.
-    Sampled rows against the oracle; dk/dv through the sum rules."""
+    Sampled query rows (out, dq) and key rows of one key/value head (dk, dv:
+    every row of its four query heads enters them) at rank and chunk edges
+    against the oracle; the sum rules for dk and dv over every head."""
     from test_parity_gpu import check
     sh = HYBRID_S65536
     q, k, v, do = attn_inputs(sh)
@@ -139,8 +141,17 @@ def test_hybrid_ring4_ulysses2_full_size_sampled():
     rows += [(0, 17, s) for s in (0, 16383, 16384, 32767, 32768, 49152, 65535)]  # rank edges
     o_ref, _ = oracle.fwd_rows(q, k, v, rows)
     check("out rows", torch.stack([out[b, s, h].cpu() for b, h, s in rows]), o_ref)
-    dq_ref = oracle.dq_rows(q, k, v, do, rows[:16])
-    check("dq rows", torch.stack([dq[b, s, h].cpu() for b, h, s in rows[:16]]), dq_ref)
+    g2 = torch.Generator().manual_seed(3)
+    qrows = rows + [(0, int(h), int(s)) for h, s in zip(torch.randint(0, sh.Hq, (17,), generator=g2),
+                                                        torch.randint(0, sh.S, (17,), generator=g2))]
+    dq_ref = oracle.dq_rows(q, k, v, do, qrows)
+    check("dq rows", torch.stack([dq[b, s, h].cpu() for b, h, s in qrows]), dq_ref)
+    # kv head 5 lives in head group 1 after the exchange (kv heads 4..7)
+    krows = [(0, 5, s) for s in (0, 1, 8191, 8192, 16383, 16384, 24575, 32767, 32768, 40960, 49151,
+                                 49152, 57344, 65534, 65535)]
+    dk_ref, dv_ref = oracle.dkv_rows(q, k, v, do, krows)
+    check("dk rows", torch.stack([dk[b, s, h].cpu() for b, h, s in krows]), dk_ref)
+    check("dv rows", torch.stack([dv[b, s, h].cpu() for b, h, s in krows]), dv_ref)
     G = sh.Hq // sh.Hkv
     do_grp = do.float().reshape(sh.B, sh.S, sh.Hkv, G, sh.D).sum(dim=(1, 3)).to(dv.device)
     dv_sum = dv.float().sum(dim=1)
