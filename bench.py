@@ -467,6 +467,22 @@ def measure_e2e(ctx, dev, sh, host_inputs, ws, steps, barrier, world):
     for k in range(2):
         run(k)
     barrier()
+    # the copies alone, outside the timed region: the link's bandwidth on this machine
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(h2d_s):
+        c0.record(h2d_s)
+        for d, h in zip(d_in[0], h_in):
+            d.copy_(h, non_blocking=True)
+        c1.record(h2d_s)
+    barrier()
+    h2d_ms = c0.elapsed_time(c1)
+    with torch.cuda.stream(d2h_s):
+        c0.record(d2h_s)
+        for h, d in zip(h_out[0], d_out[0]):
+            h.copy_(d, non_blocking=True)
+        c1.record(d2h_s)
+    barrier()
+    d2h_ms = c0.elapsed_time(c1)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(compute)
     h2d_s.wait_event(e0)
@@ -481,6 +497,8 @@ def measure_e2e(ctx, dev, sh, host_inputs, ws, steps, barrier, world):
     d2h = sum(t.numel() * t.element_size() for t in h_out[0])
     return {"value": replica_throughput(flops_step, steps, ems, world), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems / steps,
+            "copies_alone": {"h2d_ms": h2d_ms, "h2d_gbs": h2d / (h2d_ms / 1e3) / 1e9,
+                             "d2h_ms": d2h_ms, "d2h_gbs": d2h / (d2h_ms / 1e3) / 1e9},
             "overlap": "copies on their own streams, inputs/outputs double-buffered; the forward starts "
                        "once q, k, v are in, out and lse are copied back during the backward",
             "gpu_launches": 4 * steps}

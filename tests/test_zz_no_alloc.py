@@ -41,13 +41,13 @@ def lib():
     return lib
 
 
-def _noalloc(lib, q, k, v, out, lse, do, P):
+def _noalloc(lib, q, k, v, out, lse, do, P, causal=False):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     d = ctx._desc
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     rc = lib.ctx_attn_bwd_noalloc(ctypes.byref(d(q)), ctypes.byref(d(k)), ctypes.byref(d(v)),
                                   ctypes.byref(d(out)), ctypes.c_void_p(lse.data_ptr()),
-                                  ctypes.byref(d(do)), P, None, 0, 0, 0.0, ctypes.byref(d(dq)),
+                                  ctypes.byref(d(do)), P, None, 0, int(causal), 0.0, ctypes.byref(d(dq)),
                                   ctypes.byref(d(dk)), ctypes.byref(d(dv)), stream)
     return rc, (dq, dk, dv)
 
@@ -94,4 +94,38 @@ def test_noalloc_backward_d256_group_split(lib):
     torch.cuda.synchronize()
     for name, g, r in zip(("dq", "dk", "dv"), got, ref):
         _close(g, r, name)
+    assert ctx.device_status() == 0
+
+
+# (shape, causal): every head dimension, causal or not; the D=256 cases split
+# the GQA group over CTAs and keep the partial dK/dV in the scratch as well
+CASES = [(AttnShape(B=1, S=777, Hq=4, Hkv=2, D=64, P=3), True),
+         (AttnShape(B=2, S=600, Hq=2, Hkv=2, D=128, P=2), True),
+         (AttnShape(B=1, S=1024, Hq=24, Hkv=4, D=256, P=2), True),
+         (AttnShape(B=1, S=1000, Hq=12, Hkv=2, D=256, P=3), False)]
+
+
+def test_noalloc_calls_in_a_row_leave_nothing_behind(lib):
+    """The scratch keeps the last call's contents.  Calls of different head
+    dimensions, causal or not, made one after the other (each problem twice,
+    and the first problem again at the end) must each give what the regular
+    backward gives: nothing a previous call left in the array may leak into
+    the next."""
+    refs = []
+    for i, (sh, causal) in enumerate(CASES):
+        assert lib.ctx_attn_workspace_size(sh.B, sh.S, sh.Hq, sh.Hkv, sh.D, sh.P, 0) <= 64 * 1024 * 1024
+        q, k, v, do = (t.cuda() for t in attn_inputs(sh, seed=40 + i))
+        out, lse = ctx.attn_fwd(q, k, v, sh.P, causal=causal)
+        ref = ctx.attn_bwd(q, k, v, out, lse, do, sh.P, causal=causal)
+        refs.append(((q, k, v, out, lse, do), ref))
+    torch.cuda.synchronize()
+    order = [0, 0, 1, 1, 2, 2, 3, 3, 0]
+    for n, i in enumerate(order):
+        (q, k, v, out, lse, do), ref = refs[i]
+        sh, causal = CASES[i]
+        rc, got = _noalloc(lib, q, k, v, out, lse, do, sh.P, causal)
+        assert rc == 0, ctx._status_text(rc)
+        torch.cuda.synchronize()
+        for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+            _close(g, r, f"{name} (call {n + 1}: D={sh.D}, causal={causal})")
     assert ctx.device_status() == 0
