@@ -222,12 +222,15 @@ __global__ void exchange_kernel(const uint16_t* __restrict__ x, uint16_t* __rest
 // Row statistics for the backward, written in tile-major order
 // [B][Hq][ntiles][128]: delta = sum_d dO o O (fp32) and lse * log2(e).
 // Slots past a chunk's end get delta 0 and lse +inf, which makes their
-// probabilities exactly 0 in the backward kernel.
+// probabilities exactly 0 in the backward kernel.  Each thread also zeroes
+// its 8 columns of the row's fp32 dQ accumulator (tile-major
+// [B][Hq][ntiles][D/4][128][4]), which the backward kernel adds into.
 __global__ void bwd_stats_kernel(const __nv_bfloat16* __restrict__ out, int64_t osb, int64_t oss,
                                  int64_t osh, const __nv_bfloat16* __restrict__ dout, int64_t dsb,
                                  int64_t dss, int64_t dsh, const float* __restrict__ lse,
                                  float* __restrict__ lse2_t, float* __restrict__ delta_t,
-                                 const ChunkTable ct, int Hq, int S, int D, int64_t nslots) {
+                                 float* __restrict__ dq_acc, const ChunkTable ct, int Hq, int S, int D,
+                                 int64_t nslots) {
     const int tpr = D / 8;  // threads per row, 8 elements each
     const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t slot = gt / tpr;
@@ -236,6 +239,12 @@ __global__ void bwd_stats_kernel(const __nv_bfloat16* __restrict__ out, int64_t 
     const int64_t sl = in_range ? slot : 0;
     const int rr = (int)(sl % kTile);
     const int64_t bht = sl / kTile;
+    if (in_range) {
+        float* tile = dq_acc + bht * kTile * D;
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4*>(tile + ((int64_t)(2 * part) * kTile + rr) * 4) = z;
+        *reinterpret_cast<float4*>(tile + ((int64_t)(2 * part + 1) * kTile + rr) * 4) = z;
+    }
     const int t = (int)(bht % ct.ntiles);
     const int64_t bh = bht / ct.ntiles;
     const int h = (int)(bh % Hq), b = (int)(bh / Hq);
@@ -717,14 +726,14 @@ int ctx_attn_bwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
                 p.B, p.S, p.Hq, p.Hkv, (int)D, P, p.causal, p.ct.ntiles, (long long)bwd_ctas,
                 D == 256 ? "attn_bwd256_kernel, column halves" : "attn_bwd_kernel, one KV tile per CTA",
                 p.hsplit, p.head_major ? "head-major" : "tile-major");
-    if (cudaMemsetAsync(dq_acc, 0, slots * D * 4, s) != cudaSuccess) return CTX_ERR_CUDA;
     {
+        // row statistics, and the fp32 dQ accumulator zeroed
         const int64_t threads = (int64_t)slots * (D / 8);
         const int blk = 256;
         bwd_stats_kernel<<<(unsigned)((threads + blk - 1) / blk), blk, 0, s>>>(
             static_cast<const __nv_bfloat16*>(to.data), to.sb, to.ss, to.sh,
             static_cast<const __nv_bfloat16*>(tdo.data), tdo.sb, tdo.ss, tdo.sh, lse, lse2_t,
-            delta_t, p.ct, (int)Hq, (int)S, (int)D, (int64_t)slots);
+            delta_t, dq_acc, p.ct, (int)Hq, (int)S, (int)D, (int64_t)slots);
         if ((rc = launch_status())) return rc;
     }
     prof_record(1, 0, s);
