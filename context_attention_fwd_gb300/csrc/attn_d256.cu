@@ -6,7 +6,8 @@
 // and a 128 x 256 fp32 accumulator fills half of TMEM, so:
 //   * forward: one 128-row query tile per CTA; TMEM holds two score buffers
 //     (S_0, S_1: 128 columns each) and O (256 columns), so S(j+1) is computed
-//     while the softmax of tile j runs.  K and V stream through a ring of
+//     while the softmax of tile j runs; two threads issue the products (S
+//     from one, PV from the other) so that both reach the tensor core at once.  K and V stream through a ring of
 //     32 KB slots: K(j) as two column halves (the two halves of the QK^T
 //     contraction), V(j) as two 64-row halves (the two halves of the PV
 //     contraction, N = 256 each).
@@ -68,10 +69,12 @@ struct F256Bars {
     // complete two phases and its parity would no longer identify tile j
     uint64_t p_full[2];
     uint64_t pv_done;    // one completion per PV product
+    uint64_t pv_buf[2];  // PV(j) done, per score buffer j mod 2 (S(j+2) may overwrite P(j))
     uint64_t o_done;     // the last PV of a chunk (partials) or of the walk
-    uint64_t drain;
+    uint64_t drain, drain_s;
 };
-constexpr int kF256Threads = 256;  // warp 0 loads, warp 1 TMEM + MMA, warps 4..7 softmax
+// warp 0 loads, warp 1 TMEM + PV products, warp 2 S products, warps 4..7 softmax
+constexpr int kF256Threads = 256;
 constexpr float kRescaleThreshold = 8.0f;
 
 template <bool kPartials, bool kHeadMajor>
@@ -109,8 +112,11 @@ __global__ void __launch_bounds__(kF256Threads, 1) attn_fwd256_kernel(const __gr
         mbar_init(smem_u32(&bars.p_full[0]), 128);  // every softmax thread
         mbar_init(smem_u32(&bars.p_full[1]), 128);
         mbar_init(smem_u32(&bars.pv_done), 1);
+        mbar_init(smem_u32(&bars.pv_buf[0]), 1);
+        mbar_init(smem_u32(&bars.pv_buf[1]), 1);
         mbar_init(smem_u32(&bars.o_done), 1);
         mbar_init(smem_u32(&bars.drain), 1);
+        mbar_init(smem_u32(&bars.drain_s), 1);
         mbar_fence_init();
     }
     if (warp == 1) {
@@ -161,66 +167,81 @@ __global__ void __launch_bounds__(kF256Threads, 1) attn_fwd256_kernel(const __gr
                     if (last[i] >= 0) drain_wait(smem_u32(&bars.full[i]), last[i], p.timeout_ns);
             }
         }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
+    } else if (warp == 1 || warp == 2) {
+        // ---------------------------------------------------------- MMA issuers
+        // Two issuing threads.  Warp 2 issues S(j) = Q K(j)^T into score buffer
+        // j mod 2 as soon as that buffer is free (PV(j-2) has read P(j-2));
+        // warp 1 issues PV(j) once the softmax has written P(j).  S(j+1) and
+        // PV(j) thus reach the tensor core from two threads at once, which it
+        // runs at its full rate; one thread issuing both in turn left it idle
+        // between products.
         if (lane == 0) {
             constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
             constexpr uint32_t id_pv = idesc_bf16_f32(128, kD, false, true);
             const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
             const uint64_t dk0 = sdesc_sw128(sRing, 16, 1024);
             const uint64_t dv0 = sdesc_sw128(sRing, kBox / 2, 1024);  // 64-column blocks of 64 rows
-            bool ok = mbar_wait(smem_u32(&bars.q_full), 0, wc);
             auto wait_full = [&](int n) {
                 return mbar_wait(smem_u32(&bars.full[n % L::SLOTS]), (n / L::SLOTS) & 1, wc);
             };
-            auto issue_s = [&](int j) -> bool {  // S(j) = Q K(j)^T into buffer j mod 2
-                const int n0 = j * L::LOADS;
-                const uint32_t d = tmem + L::TM_S + (j & 1) * 128;
-                for (int e = 0; e < 2; ++e) {
-                    if (!wait_full(n0 + e)) return false;
-                    tc_fence_after();
-                    const uint64_t bk = dk0 + ((((n0 + e) % L::SLOTS) * kSlot) >> 4);
+            bool ok = true;
+            if (warp == 2) {
+                auto issue_s = [&](int j) -> bool {  // S(j) = Q K(j)^T into buffer j mod 2
+                    const int n0 = j * L::LOADS;
+                    const uint32_t d = tmem + L::TM_S + (j & 1) * 128;
+                    for (int e = 0; e < 2; ++e) {
+                        if (!wait_full(n0 + e)) return false;
+                        tc_fence_after();
+                        const uint64_t bk = dk0 + ((((n0 + e) % L::SLOTS) * kSlot) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ss(d, dq0 + kmajor_koff(8 * e + kk), bk + kmajor_koff(kk), id_s,
-                               (e > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_ss(d, dq0 + kmajor_koff(8 * e + kk), bk + kmajor_koff(kk), id_s,
+                                   (e > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(smem_u32(&bars.s_full[j & 1]));
+                    mma_commit(smem_u32(&bars.empty[n0 % L::SLOTS]));
+                    mma_commit(smem_u32(&bars.empty[(n0 + 1) % L::SLOTS]));
+                    return true;
+                };
+                ok = mbar_wait(smem_u32(&bars.q_full), 0, wc);
+                for (int j = 0; j < n_kv && ok; ++j) {
+                    // buffer j mod 2 holds P(j-2) until PV(j-2) has read it
+                    if (j >= 2 && !(ok = mbar_wait(smem_u32(&bars.pv_buf[j & 1]), ((j - 2) >> 1) & 1, wc))) break;
+                    ok = issue_s(j);
                 }
-                mma_commit(smem_u32(&bars.s_full[j & 1]));
-                mma_commit(smem_u32(&bars.empty[n0 % L::SLOTS]));
-                mma_commit(smem_u32(&bars.empty[(n0 + 1) % L::SLOTS]));
-                return true;
-            };
-            if (ok) ok = issue_s(0);
-            if (ok && n_kv > 1) ok = issue_s(1);
-            KvWalk w;
-            kv_first(ct, g, w);
-            for (int j = 0; j < n_kv && ok; ++j, kv_next(ct, g, w)) {
-                const bool first_c = w.t == w.t0, last_c = kv_chunk_last(ct, g, w);
-                const bool acc0 = kPartials ? !first_c : j > 0;
-                if (!(ok = mbar_wait(smem_u32(&bars.p_full[j & 1]), (j >> 1) & 1, wc))) break;
-                tc_fence_after();
-                const int n0 = j * L::LOADS + 2;
-                const uint32_t pa = tmem + L::TM_S + (j & 1) * 128;  // P(j), bf16 pairs
-                for (int e = 0; e < 2; ++e) {  // O += P[:, 64e:64e+64] V[64e:64e+64, :]
-                    if (!(ok = wait_full(n0 + e))) break;
+                if (!ok) abort_flag = 1;
+                mma_commit(smem_u32(&bars.drain_s));
+                drain_wait(smem_u32(&bars.drain_s), 0, p.timeout_ns);
+            } else {
+                KvWalk w;
+                kv_first(ct, g, w);
+                for (int j = 0; j < n_kv && ok; ++j, kv_next(ct, g, w)) {
+                    const bool first_c = w.t == w.t0, last_c = kv_chunk_last(ct, g, w);
+                    const bool acc0 = kPartials ? !first_c : j > 0;
+                    if (!(ok = mbar_wait(smem_u32(&bars.p_full[j & 1]), (j >> 1) & 1, wc))) break;
                     tc_fence_after();
-                    const uint64_t bv = dv0 + ((((n0 + e) % L::SLOTS) * kSlot) >> 4);
+                    const int n0 = j * L::LOADS + 2;
+                    const uint32_t pa = tmem + L::TM_S + (j & 1) * 128;  // P(j), bf16 pairs
+                    for (int e = 0; e < 2; ++e) {  // O += P[:, 64e:64e+64] V[64e:64e+64, :]
+                        if (!(ok = wait_full(n0 + e))) break;
+                        tc_fence_after();
+                        const uint64_t bv = dv0 + ((((n0 + e) % L::SLOTS) * kSlot) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_ts(tmem + L::TM_O, pa + 32 * e + 8 * kk, bv + kk * (2048 >> 4), id_pv,
-                               (acc0 || e > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ts(tmem + L::TM_O, pa + 32 * e + 8 * kk, bv + kk * (2048 >> 4), id_pv,
+                                   (acc0 || e > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    if (!ok) break;
+                    mma_commit(smem_u32(&bars.empty[n0 % L::SLOTS]));
+                    mma_commit(smem_u32(&bars.empty[(n0 + 1) % L::SLOTS]));
+                    mma_commit(smem_u32(&bars.pv_done));
+                    mma_commit(smem_u32(&bars.pv_buf[j & 1]));
+                    if (kPartials ? last_c : j == n_kv - 1) mma_commit(smem_u32(&bars.o_done));
                 }
-                if (!ok) break;
-                mma_commit(smem_u32(&bars.empty[n0 % L::SLOTS]));
-                mma_commit(smem_u32(&bars.empty[(n0 + 1) % L::SLOTS]));
-                mma_commit(smem_u32(&bars.pv_done));
-                if (kPartials ? last_c : j == n_kv - 1) mma_commit(smem_u32(&bars.o_done));
-                // S(j+2) overwrites P(j): issued after the PV that reads it (in order)
-                if (j + 2 < n_kv && !(ok = issue_s(j + 2))) break;
+                if (!ok) abort_flag = 1;
+                mma_commit(smem_u32(&bars.drain));
+                drain_wait(smem_u32(&bars.drain), 0, p.timeout_ns);
             }
-            if (!ok) abort_flag = 1;
-            mma_commit(smem_u32(&bars.drain));
-            drain_wait(smem_u32(&bars.drain), 0, p.timeout_ns);
         }
     } else if (warp >= 4) {
         // ---------------------------------------------------------- softmax
