@@ -68,7 +68,7 @@ struct BwdBars {
     uint64_t s_full, dp_full, p_ready, ds_ready, ds_free, dv_done;
     uint64_t dq_full, dq_drained;
     uint64_t final_mma;
-    uint64_t drain, drain2;
+    uint64_t drain, drain2, drain3;
     uint32_t tmem_slot;
     int abort_flag;
 };
@@ -76,8 +76,8 @@ struct BwdBars {
 constexpr int kMathWarps = 8;
 constexpr int kMathThreads = 32 * kMathWarps;
 constexpr int kDrainThreads = 128;
-constexpr int kThreads = 480;
-constexpr int kProducerWarp = 12, kMmaWarp = 13, kMma2Warp = 14;
+constexpr int kThreads = 512;
+constexpr int kProducerWarp = 12, kMmaWarp = 13, kMma2Warp = 14, kMmaDpWarp = 15;
 
 __device__ __forceinline__ int pick3(int o, int s, int h, int b) {
     return o == 0 ? s : (o == 1 ? h : b);
@@ -141,6 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         mbar_init(smem_u32(&bars.dq_drained), kDrainThreads);
         mbar_init(smem_u32(&bars.final_mma), 1);
         mbar_init(smem_u32(&bars.drain), 1);
+        mbar_init(smem_u32(&bars.drain3), 1);
         mbar_fence_init();
     }
     if (warp == kMmaWarp) {
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                     if (last_ph[st] >= 0) drain_wait(smem_u32(&bars.q_full[st]), last_ph[st], p.timeout_ns);
             }
         }
-    } else if (warp == kMmaWarp || warp == kMma2Warp) {
+    } else if (warp == kMmaWarp || warp == kMma2Warp || warp == kMmaDpWarp) {
         // ---------------------------------------------------------- MMA issuers
         if (lane == 0) {
             constexpr uint32_t id_st = idesc_bf16_f32(128, 128, false, false);  // K-major A and B
@@ -216,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             auto koff = [](int kk) -> uint32_t { return ((kk >> 2) * L::BOX + (kk & 3) * 32) >> 4; };
             bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, wc);
             if (warp == kMmaWarp) {
-                // S_i = K Q_i^T and dP_i = V dO_i^T, per query tile
+                // S_i = K Q_i^T, per query tile
                 auto issue_s = [&](int st) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
@@ -225,24 +226,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                     mma_commit(smem_u32(&bars.s_full));
                 };
                 if (ok && (ok = mbar_wait(smem_u32(&bars.q_full[0]), 0, wc))) issue_s(0);
+                for (int i = 0; i + 1 < n_q && ok; ++i) {
+                    // S^T_{i+1} overwrites P^T_i: wait until dV_i has read it
+                    if (!(ok = mbar_wait(smem_u32(&bars.dv_done), i & 1, wc))) break;
+                    if (!(ok = mbar_wait(smem_u32(&bars.q_full[(i + 1) & 1]), ((i + 1) >> 1) & 1, wc))) break;
+                    tc_fence_after();
+                    issue_s((i + 1) & 1);
+                }
+                mma_commit(smem_u32(&bars.drain));
+                drain_wait(smem_u32(&bars.drain), 0, p.timeout_ns);
+            } else if (warp == kMmaDpWarp) {
+                // dP_i = V dO_i^T, per query tile, from its own thread: S_{i+1}
+                // does not wait behind dP_i, which waits for the drain of dQ_{i-1}
                 for (int i = 0; i < n_q && ok; ++i) {
                     const int st = i & 1;
-                    // dP^T = V dO^T, into the columns dQ_{i-1} occupied once it is drained
+                    if (!(ok = mbar_wait(smem_u32(&bars.q_full[st]), (i >> 1) & 1, wc))) break;
+                    // into the columns dQ_{i-1} occupied once it is drained
                     if (i > 0 && !(ok = mbar_wait(smem_u32(&bars.dq_drained), (i - 1) & 1, wc))) break;
+                    tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
                         mma_ss(tmem + L::TM_DP, dV_k + koff(kk), dO_k + st * kStage + koff(kk), id_st,
                                kk > 0 ? 1u : 0u);
                     mma_commit(smem_u32(&bars.dp_full));
-                    // S^T_{i+1} overwrites P^T_i: wait until dV_i has read it
-                    if (i + 1 < n_q) {
-                        if (!(ok = mbar_wait(smem_u32(&bars.dv_done), i & 1, wc))) break;
-                        if (!(ok = mbar_wait(smem_u32(&bars.q_full[(i + 1) & 1]), ((i + 1) >> 1) & 1, wc))) break;
-                        issue_s((i + 1) & 1);
-                    }
                 }
-                mma_commit(smem_u32(&bars.drain));
-                drain_wait(smem_u32(&bars.drain), 0, p.timeout_ns);
+                mma_commit(smem_u32(&bars.drain3));
+                drain_wait(smem_u32(&bars.drain3), 0, p.timeout_ns);
             } else {
                 // dV_i += P^T dO, dK_i += dS^T Q, dQ_i = dS K, per query tile
                 for (int i = 0; i < n_q && ok; ++i) {
