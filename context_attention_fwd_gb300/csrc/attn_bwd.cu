@@ -22,18 +22,20 @@
 // dQ tiles are added into an fp32 accumulator in global memory (vector
 // reductions); dK, dV stay in TMEM for the whole CTA and are written once.
 //
-// Warp roles (480 threads):
+// Warp roles (512 threads):
 //   warps 0..7   P / dS math: one KV row per thread (TMEM lane quarter =
 //                warp mod 4), warps 0..3 take query columns 0..63 and warps
 //                4..7 columns 64..127; dV epilogue (half the columns each)
 //   warps 8..11  dQ drain (one query row per thread); dK epilogue
 //   warp 12      TMA producer (K, V once; Q, dO, lse, delta per query tile, 2 stages)
-//   warp 13      TMEM owner; issues S and dP (the products that feed the math)
+//   warp 13      TMEM owner; issues S (the product that feeds the softmax)
+//   warp 15      issues dP (the product that feeds dS)
 //   warp 14      issues dV, dK and dQ (the products that consume the math)
-// Two MMA issuers keep the tensor core fed: while one waits on a barrier,
-// the products the other has queued keep running.  Their TMEM hazards are
-// ordered explicitly: S_{i+1} waits until dV_i (which reads P^T_i from the S
-// columns) is done, dP_{i+1} until dQ_i (written over dP_i) has been drained.
+// Three MMA issuers keep the tensor core fed: while one waits on a barrier,
+// the products the others have queued keep running, and S_{i+1} never waits
+// behind dP_i.  Their TMEM hazards are ordered explicitly: S_{i+1} waits
+// until dV_i (which reads P^T_i from the S columns) is done, dP_{i+1} until
+// dQ_i (written over dP_i) has been drained.
 // P^T is written back into the S^T columns it was computed from (bf16
 // pairs): columns 0..31 for query columns 0..63, columns 96..127 for query
 // columns 64..127, so the two math warps of a lane quarter never overwrite
