@@ -179,7 +179,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             bool ok = true;
             const int skip = debug_skip_step(p.debug, n_q);  // -1 in normal use
             for (int i = 0; i < n_q; ++i, next(q)) {
-                if (i == skip) continue;  // failure injection: Q_i, dO_i never arrive
+                if (i == skip) {  // failure injection: no Q, dO from query tile i on
+                    ok = false;
+                    break;
+                }
                 const int st = i & 1, ph = (i >> 1) & 1;
                 if (!(ok = mbar_wait(smem_u32(&bars.q_empty[st]), ph ^ 1, wc))) break;
                 const uint32_t qf = smem_u32(&bars.q_full[st]);

@@ -73,7 +73,7 @@ struct F256Bars {
     uint64_t o_done;     // the last PV of a chunk (partials) or of the walk
     uint64_t drain, drain_s;
 };
-// warp 0 loads, warp 1 TMEM + PV products, warp 2 S products, warps 4..7 softmax
+// warps 0 and 3 load, warp 1 TMEM + PV products, warp 2 S products, warps 4..7 softmax
 constexpr int kF256Threads = 256;
 constexpr float kRescaleThreshold = 8.0f;
 
@@ -128,15 +128,23 @@ __global__ void __launch_bounds__(kF256Threads, 1) attn_fwd256_kernel(const __gr
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
 
-    if (warp == 0) {
-        // ---------------------------------------------------------- producer
+    if (warp == 0 || warp == 3) {
+        // ---------------------------------------------------------- producers
+        // Two loading threads: one thread's bulk copies stream at about 35 B per
+        // clock into its CTA, two at twice that.  Each ring slot belongs to one
+        // of them (warp 0: even slots, warp 3: odd slots), so the loads of a
+        // slot are issued in order and a slot's empty barrier is never waited
+        // on more than one phase ahead.
         if (lane == 0) {
-            tma_prefetch_desc(&p.tq.map);
+            const int me = warp == 0 ? 0 : 1;
             tma_prefetch_desc(&p.tk.map);
             tma_prefetch_desc(&p.tv.map);
             const uint32_t qf = smem_u32(&bars.q_full);
-            mbar_arrive_expect_tx(qf, 4 * kBox);
-            for (int e = 0; e < 4; ++e) tma_tile(p.tq, sQ + e * kBox, qf, e * 64, q_start, h, b);
+            if (me == 0) {
+                tma_prefetch_desc(&p.tq.map);
+                mbar_arrive_expect_tx(qf, 4 * kBox);
+                for (int e = 0; e < 4; ++e) tma_tile(p.tq, sQ + e * kBox, qf, e * 64, q_start, h, b);
+            }
             int last[L::SLOTS];
             for (int i = 0; i < L::SLOTS; ++i) last[i] = -1;
             bool ok = true;
@@ -144,10 +152,14 @@ __global__ void __launch_bounds__(kF256Threads, 1) attn_fwd256_kernel(const __gr
             KvWalk w;
             kv_first(ct, g, w);
             for (int j = 0; j < n_kv && ok; ++j, kv_next(ct, g, w)) {
-                if (j == skip) continue;  // failure injection: K(j), V(j) never arrive
+                if (j == skip) {  // failure injection: no K, V from step j on
+                    ok = false;
+                    break;
+                }
                 const int kv_start = ct.off[w.c] + (w.t - w.t0) * kTile;
                 for (int k = 0; k < L::LOADS; ++k) {
                     const int n = j * L::LOADS + k, slot = n % L::SLOTS, ph = (n / L::SLOTS) & 1;
+                    if ((slot & 1) != me) continue;
                     if (!(ok = mbar_wait(smem_u32(&bars.empty[slot]), ph ^ 1, wc))) break;
                     const uint32_t f = smem_u32(&bars.full[slot]), dst = sRing + slot * kSlot;
                     mbar_arrive_expect_tx(f, kSlot);
@@ -162,7 +174,7 @@ __global__ void __launch_bounds__(kF256Threads, 1) attn_fwd256_kernel(const __gr
                 }
             }
             if (!ok) {
-                drain_wait(qf, 0, p.timeout_ns);
+                if (me == 0) drain_wait(qf, 0, p.timeout_ns);
                 for (int i = 0; i < L::SLOTS; ++i)
                     if (last[i] >= 0) drain_wait(smem_u32(&bars.full[i]), last[i], p.timeout_ns);
             }
@@ -423,8 +435,8 @@ struct B256Bars {
 };
 static_assert(sizeof(B256Bars) <= 256, "barrier block");
 constexpr int kB256MathWarps = 8, kB256MathThreads = 256, kB256DrainThreads = 128;
-constexpr int kB256Threads = 480;
-constexpr int kB256Producer = 12, kB256MmaX = 13, kB256MmaY = 14;
+constexpr int kB256Threads = 512;
+constexpr int kB256Producer = 12, kB256MmaX = 13, kB256MmaY = 14, kB256Producer2 = 15;
 
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
@@ -436,7 +448,11 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 //   3: Q[:, half h] (+ lse2, delta)   4: V[:, half h]   5: dO[:, half h]
 // Load n goes to slot n mod 4 and waits for the release of load n - 4; the
 // releases happen in the order S part A (0), dP part A (1, 2), dK (3),
-// dP part B (4), dV (5), so no load waits on a product that needs it.
+// dP part B (4), dV (5), so no load waits on a product that needs it.  Two
+// threads issue the loads (one thread's bulk copies stream at about 35 B per
+// clock into its CTA, two at twice that): warp 12 those of slots 0 and 2,
+// warp 15 those of slots 1 and 3, each in load order, so the loads of a slot
+// stay in order and its empty barrier is never waited on a phase ahead.
 template <bool kHeadMajor>
 __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __grid_constant__ BwdParams p) {
     using L = B256;
@@ -503,25 +519,32 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
     auto full_bar = [&](int n) { return smem_u32(&bars.full[n % L::SLOTS]); };
     auto empty_bar = [&](int n) { return smem_u32(&bars.empty[n % L::SLOTS]); };
 
-    if (warp == kB256Producer) {
-        // ---------------------------------------------------------- producer
+    if (warp == kB256Producer || warp == kB256Producer2) {
+        // ---------------------------------------------------------- producers
         if (lane == 0) {
+            const int me = warp == kB256Producer ? 0 : 1;
             tma_prefetch_desc(&p.tq.map);
-            tma_prefetch_desc(&p.tk.map);
             tma_prefetch_desc(&p.tv.map);
             tma_prefetch_desc(&p.tdo.map);
             const uint32_t kf = smem_u32(&bars.k_full);
-            mbar_arrive_expect_tx(kf, 4 * kBox);
-            for (int e = 0; e < 4; ++e) tma_tile(p.tk, sK + e * kBox, kf, e * 64, kv_start, hk, b);
+            if (me == 0) {
+                tma_prefetch_desc(&p.tk.map);
+                mbar_arrive_expect_tx(kf, 4 * kBox);
+                for (int e = 0; e < 4; ++e) tma_tile(p.tk, sK + e * kBox, kf, e * 64, kv_start, hk, b);
+            }
             QTileIter q = q0;
             int last[L::SLOTS] = {-1, -1, -1, -1};
             bool ok = true;
             const int skip = debug_skip_step(p.debug, n_q);  // -1 in normal use
             for (int i = 0; i < n_q && ok; ++i, qw.next(q)) {
-                if (i == skip) continue;  // failure injection: query tile i's loads never arrive
+                if (i == skip) {  // failure injection: no loads from query tile i on
+                    ok = false;
+                    break;
+                }
                 const int q_start = qw.first_row(q);
                 for (int k = 0; k < L::LOADS; ++k) {
                     const int n = i * L::LOADS + k;
+                    if ((slot_of(n) & 1) != me) continue;
                     if (!(ok = mbar_wait(empty_bar(n), phase_of(n) ^ 1, wc))) break;
                     const uint32_t f = full_bar(n), dst = sRing + slot_of(n) * kSlot;
                     const int half = k < 3 ? 1 - hh : hh;
@@ -540,7 +563,7 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
                 }
             }
             if (!ok) {
-                drain_wait(kf, 0, p.timeout_ns);
+                if (me == 0) drain_wait(kf, 0, p.timeout_ns);
                 for (int s = 0; s < L::SLOTS; ++s)
                     if (last[s] >= 0) drain_wait(smem_u32(&bars.full[s]), last[s], p.timeout_ns);
             }

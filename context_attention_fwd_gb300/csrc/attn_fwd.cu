@@ -157,7 +157,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             KvWalk w;
             kv_first(ct, g, w);
             for (int j = 0; j < n_kv; ++j, kv_next(ct, g, w)) {
-                if (j == skip) continue;  // failure injection: K(j), V(j) never arrive
+                if (j == skip) {  // failure injection: no K, V from step j on
+                    ok = false;
+                    break;
+                }
                 const int st = j & 1, ph = (j >> 1) & 1;
                 const int kv_start = ct.off[w.c] + (w.t - w.t0) * kTile;
                 if (!(ok = mbar_wait(smem_u32(&bars.k_empty[st]), ph ^ 1, wc))) break;

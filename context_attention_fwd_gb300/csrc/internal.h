@@ -16,14 +16,17 @@ constexpr int kMaxChunks = 64;
 constexpr int kTile = 128;  // rows of a query or key/value tile
 
 // Test-only switches carried by the parameter blocks (values of the
-// CTX_DEBUG_* bits of the C ABI).  kDebugSkipArrival: the TMA producer of
-// the attention kernel leaves out the loads (and their mbarrier arrival) of
-// its second load step, so a consumer's bounded wait runs out and the
-// kernel takes its abort path.
+// CTX_DEBUG_* bits of the C ABI).  kDebugSkipArrival: the TMA producers of
+// the attention kernel issue no loads (and so no mbarrier arrivals) from
+// their second load step on, so a consumer's bounded wait runs out and the
+// kernel takes its abort path.  The producers stop rather than leave out a
+// single step: with one step missing, the later loads into a ring slot
+// would wait on an empty barrier that lags one phase behind, which a parity
+// wait cannot tell from a completed release, and would overrun the slot.
 constexpr int kDebugSkipArrival = 1;
 
-// Index of the load step a producer leaves out under kDebugSkipArrival, or
-// -1: the second of n steps (the first when there is only one).
+// Index of the load step at which a producer stops under kDebugSkipArrival,
+// or -1: the second of n steps (the first when there is only one).
 __host__ __device__ inline int debug_skip_step(int debug, int n) {
     return (debug & kDebugSkipArrival) ? (n > 1 ? 1 : 0) : -1;
 }

@@ -238,9 +238,9 @@ int ctx_profile_read(int kernel, double* total_ms, int* launches);
  * ctx_debug_set(flags, wait_limit_ms) applies to the attention calls made
  * after it, process-wide, until it is called again; ctx_debug_set(0, 0)
  * restores normal operation.
- *  CTX_DEBUG_SKIP_ARRIVAL: the TMA producer of every attention kernel
- *    (forward and backward, every head dimension) leaves out the loads of its
- *    second load step and their mbarrier arrival.  A consumer's bounded wait
+ *  CTX_DEBUG_SKIP_ARRIVAL: the TMA producers of every attention kernel
+ *    (forward and backward, every head dimension) issue no loads, and so no
+ *    mbarrier arrivals, from their second load step on.  A consumer's bounded wait
  *    then runs out; the kernel records CTX_ERR_TIMEOUT in the device status
  *    word, waits (bounded) for its own copies and products in flight, frees
  *    its tensor memory and returns, with its outputs incomplete.  Nothing

@@ -1,9 +1,9 @@
 """Failure detection in the attention kernels themselves, on the GPU.
 
 Every device-side wait of the attention kernels is bounded.  With the
-test-only switch CTX_DEBUG_SKIP_ARRIVAL the TMA producer of each kernel
-leaves out the loads of its second load step and their mbarrier arrival, so
-a consumer's wait runs out: the kernel must record CTX_ERR_TIMEOUT in the
+test-only switch CTX_DEBUG_SKIP_ARRIVAL the TMA producers of each kernel
+issue no loads (and so no mbarrier arrivals) from their second load step on,
+so a consumer's wait runs out: the kernel must record CTX_ERR_TIMEOUT in the
 device status word, leave its loops, wait (bounded) for its own copies and
 products in flight, free its tensor memory and return.  Nothing faults,
 traps or hangs; the test then runs the same call normally and holds it to
