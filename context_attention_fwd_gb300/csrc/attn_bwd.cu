@@ -312,11 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             if (!(ok = mbar_wait(smem_u32(&bars.s_full), i & 1, wc))) break;
             tc_fence_after();
             uint32_t pr[64];
-            tmem_ld32(taddr + s_cols, pr);
-            tmem_ld32(taddr + s_cols + 32, pr + 32);
-            tmem_ld_wait();
-            reg_fence32(pr);
-            reg_fence32(pr + 32);
+            tmem_ld64_sync(taddr + s_cols, pr);
             // P^T (fp32 kept in pr); padded query columns have lse2 = +inf -> 0
 #pragma unroll
             for (int k4 = 0; k4 < 16; ++k4) {
@@ -350,9 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 uint32_t dp[32];
-                tmem_ld32(taddr + L::TM_DP + half * 64 + cc * 32, dp);
-                tmem_ld_wait();
-                reg_fence32(dp);
+                tmem_ld32_sync(taddr + L::TM_DP + half * 64 + cc * 32, dp);
                 uint32_t w[16];
 #pragma unroll
                 for (int k4 = 0; k4 < 8; ++k4) {
@@ -389,9 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
 #pragma unroll
             for (int cc = 0; cc < kHalfCols / 32; ++cc) {
                 uint32_t o[32];
-                tmem_ld32(taddr + L::TM_DV + half * kHalfCols + cc * 32, o);
-                tmem_ld_wait();
-                reg_fence32(o);
+                tmem_ld32_sync(taddr + L::TM_DV + half * kHalfCols + cc * 32, o);
                 if (row_valid) {
                     uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
 #pragma unroll
@@ -420,11 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
 #pragma unroll
             for (int hc = 0; hc < D / 64; ++hc) {
                 uint32_t v[64];
-                tmem_ld32(taddr + L::TM_DP + hc * 64, v);
-                tmem_ld32(taddr + L::TM_DP + hc * 64 + 32, v + 32);
-                tmem_ld_wait();
-                reg_fence32(v);
-                reg_fence32(v + 32);
+                tmem_ld64_sync(taddr + L::TM_DP + hc * 64, v);
                 if (hc == D / 64 - 1) {
                     tc_fence_before();
                     mbar_arrive(smem_u32(&bars.dq_drained));
@@ -446,9 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t o[32];
-                tmem_ld32(taddr + L::TM_DK + cc * 32, o);
-                tmem_ld_wait();
-                reg_fence32(o);
+                tmem_ld32_sync(taddr + L::TM_DK + cc * 32, o);
                 if (row_valid) {
                     uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
 #pragma unroll

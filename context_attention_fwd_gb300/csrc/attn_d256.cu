@@ -276,15 +276,7 @@ __global__ void __launch_bounds__(kF256Threads, 1) attn_fwd256_kernel(const __gr
             if (!(ok = mbar_wait(smem_u32(&bars.s_full[j & 1]), (j >> 1) & 1, wc))) break;
             tc_fence_after();
             uint32_t s[128];
-            tmem_ld32(taddr + s_cols + 0, s);
-            tmem_ld32(taddr + s_cols + 32, s + 32);
-            tmem_ld32(taddr + s_cols + 64, s + 64);
-            tmem_ld32(taddr + s_cols + 96, s + 96);
-            tmem_ld_wait();
-            reg_fence32(s);
-            reg_fence32(s + 32);
-            reg_fence32(s + 64);
-            reg_fence32(s + 96);
+            tmem_ld128_sync(taddr + s_cols, s);
             if (kv_len < kTile || diag) {
 #pragma unroll
                 for (int k = 0; k < 128; ++k)
@@ -338,9 +330,7 @@ __global__ void __launch_bounds__(kF256Threads, 1) attn_fwd256_kernel(const __gr
 #pragma unroll
                 for (int cc = 0; cc < kD / 32; ++cc) {
                     uint32_t o[32];
-                    tmem_ld32(taddr + L::TM_O + cc * 32, o);
-                    tmem_ld_wait();
-                    reg_fence32(o);
+                    tmem_ld32_sync(taddr + L::TM_O + cc * 32, o);
 #pragma unroll
                     for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
                     tmem_st32(taddr + L::TM_O + cc * 32, o);
@@ -358,9 +348,7 @@ __global__ void __launch_bounds__(kF256Threads, 1) attn_fwd256_kernel(const __gr
 #pragma unroll
                 for (int cc = 0; cc < kD / 32; ++cc) {
                     uint32_t o[32];
-                    tmem_ld32(taddr + L::TM_O + cc * 32, o);
-                    tmem_ld_wait();
-                    reg_fence32(o);
+                    tmem_ld32_sync(taddr + L::TM_O + cc * 32, o);
                     if (valid) {
                         float4* dst = reinterpret_cast<float4*>(p.part_o + prow * kD + cc * 32);
 #pragma unroll
@@ -384,9 +372,7 @@ __global__ void __launch_bounds__(kF256Threads, 1) attn_fwd256_kernel(const __gr
 #pragma unroll
                 for (int cc = 0; cc < kD / 32; ++cc) {
                     uint32_t o[32];
-                    tmem_ld32(taddr + L::TM_O + cc * 32, o);
-                    tmem_ld_wait();
-                    reg_fence32(o);
+                    tmem_ld32_sync(taddr + L::TM_O + cc * 32, o);
                     if (valid) {
                         uint4* dst = reinterpret_cast<uint4*>(dst_row + cc * 32);
 #pragma unroll
@@ -453,6 +439,9 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 // clock into its CTA, two at twice that): warp 12 those of slots 0 and 2,
 // warp 15 those of slots 1 and 3, each in load order, so the loads of a slot
 // stay in order and its empty barrier is never waited on a phase ahead.
+// Q_h is read by S part B and dK, dO_h by dP part B and dV: a slot is free
+// once each product that reads it has completed (two releases per load, one
+// per reader), whichever thread then refills it.
 template <bool kHeadMajor>
 __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __grid_constant__ BwdParams p) {
     using L = B256;
@@ -486,7 +475,7 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
         mbar_init(smem_u32(&bars.k_full), 1);
         for (int i = 0; i < L::SLOTS; ++i) {
             mbar_init(smem_u32(&bars.full[i]), 1);
-            mbar_init(smem_u32(&bars.empty[i]), 1);
+            mbar_init(smem_u32(&bars.empty[i]), 2);  // two releases per load (see the producers)
         }
         mbar_init(smem_u32(&bars.s_full), 1);
         mbar_init(smem_u32(&bars.dp_full), 1);
@@ -581,6 +570,12 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
             const uint64_t dK_mn = sdesc_sw128(sK + 2 * hh * kBox, kBox, 1024);  // K[:, half h]
             constexpr uint32_t kMnStep = 2048 >> 4;
             auto ring_off = [&](int n) -> uint32_t { return (uint32_t)(slot_of(n) * kSlot) >> 4; };
+            // a slot's empty barrier completes after two releases: each product that
+            // reads the load gives one (a sole reader gives both), so a slot is
+            // refilled only after every product reading it has completed
+            auto release = [&](int n, int times) {
+                for (int t = 0; t < times; ++t) mma_commit(empty_bar(n));
+            };
             bool ok = mbar_wait(smem_u32(&bars.k_full), 0, wc);
             if (warp == kB256MmaX) {
                 // S^T = K Q^T and dP^T = V dO^T, each as two column-half contractions
@@ -594,7 +589,7 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
                     for (int kk = 0; kk < 8; ++kk)
                         mma_ss(tmem + L::TM_S, dK_k + kmajor_koff(8 * (1 - hh) + kk), dR_k + ring_off(n0) + kmajor_koff(kk),
                                id_st, kk > 0 ? 1u : 0u);
-                    mma_commit(empty_bar(n0));
+                    release(n0, 2);
                     // dP^T_i overwrites dQ_{i-1}: wait until it has been drained
                     if (i > 0 && !(ok = mbar_wait(smem_u32(&bars.dq_drained), (i - 1) & 1, wc))) break;
                     if (!(ok = mbar_wait(full_bar(n0 + 1), phase_of(n0 + 1), wc))) break;
@@ -604,8 +599,8 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
                     for (int kk = 0; kk < 8; ++kk)
                         mma_ss(tmem + L::TM_DP, dR_k + ring_off(n0 + 1) + kmajor_koff(kk),
                                dR_k + ring_off(n0 + 2) + kmajor_koff(kk), id_st, kk > 0 ? 1u : 0u);
-                    mma_commit(empty_bar(n0 + 1));
-                    mma_commit(empty_bar(n0 + 2));
+                    release(n0 + 1, 2);
+                    release(n0 + 2, 2);
                     if (!(ok = mbar_wait(full_bar(n0 + 3), phase_of(n0 + 3), wc))) break;
                     tc_fence_after();
 #pragma unroll
@@ -613,6 +608,7 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
                         mma_ss(tmem + L::TM_S, dK_k + kmajor_koff(8 * hh + kk), dR_k + ring_off(n0 + 3) + kmajor_koff(kk),
                                id_st, 1u);
                     mma_commit(smem_u32(&bars.s_full));
+                    release(n0 + 3, 1);  // Q_h: dK gives the other release
                     if (!(ok = mbar_wait(full_bar(n0 + 4), phase_of(n0 + 4), wc))) break;
                     if (!(ok = mbar_wait(full_bar(n0 + 5), phase_of(n0 + 5), wc))) break;
                     tc_fence_after();
@@ -620,7 +616,8 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
                     for (int kk = 0; kk < 8; ++kk)
                         mma_ss(tmem + L::TM_DP, dR_k + ring_off(n0 + 4) + kmajor_koff(kk),
                                dR_k + ring_off(n0 + 5) + kmajor_koff(kk), id_st, 1u);
-                    mma_commit(empty_bar(n0 + 4));
+                    release(n0 + 4, 2);
+                    release(n0 + 5, 1);  // dO_h: dV gives the other release
                     mma_commit(smem_u32(&bars.dp_full));
                 }
                 mma_commit(smem_u32(&bars.drain));
@@ -637,14 +634,14 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
                         mma_ts(tmem + L::TM_DV, tmem + L::TM_S + (kk < 4 ? kk * 8 : 96 + (kk - 4) * 8),
                                dR_mn + ring_off(n0 + 5) + kk * kMnStep, id_dv, (i > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(smem_u32(&bars.dv_done));
-                    mma_commit(empty_bar(n0 + 5));
+                    release(n0 + 5, 1);
                     if (!(ok = mbar_wait(smem_u32(&bars.ds_ready), i & 1, wc))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < kTile / 16; ++kk)
                         mma_ss(tmem + L::TM_DK, dS_k + kmajor_koff(kk), dR_mn + ring_off(n0 + 3) + kk * kMnStep, id_dk,
                                (i > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(empty_bar(n0 + 3));
+                    release(n0 + 3, 1);
 #pragma unroll
                     for (int kk = 0; kk < kTile / 16; ++kk)
                         mma_ss(tmem + L::TM_DP, dS_mn + kk * kMnStep, dK_mn + kk * kMnStep, id_dq, kk > 0 ? 1u : 0u);
@@ -678,11 +675,7 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
             if (!(ok = mbar_wait(smem_u32(&bars.s_full), i & 1, wc))) break;
             tc_fence_after();
             uint32_t pr[64];
-            tmem_ld32(taddr + s_cols, pr);
-            tmem_ld32(taddr + s_cols + 32, pr + 32);
-            tmem_ld_wait();
-            reg_fence32(pr);
-            reg_fence32(pr + 32);
+            tmem_ld64_sync(taddr + s_cols, pr);
 #pragma unroll
             for (int k4 = 0; k4 < 16; ++k4) {
                 const float4 l4 = lse2[k4];
@@ -714,9 +707,7 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 uint32_t dp[32];
-                tmem_ld32(taddr + L::TM_DP + half * 64 + cc * 32, dp);
-                tmem_ld_wait();
-                reg_fence32(dp);
+                tmem_ld32_sync(taddr + L::TM_DP + half * 64 + cc * 32, dp);
                 uint32_t wv[16];
 #pragma unroll
                 for (int k4 = 0; k4 < 8; ++k4) {
@@ -749,9 +740,7 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 uint32_t o[32];
-                tmem_ld32(taddr + L::TM_DV + half * 64 + cc * 32, o);
-                tmem_ld_wait();
-                reg_fence32(o);
+                tmem_ld32_sync(taddr + L::TM_DV + half * 64 + cc * 32, o);
                 if (row_valid && part_row) {  // fp32 partial, summed by dkv_reduce_kernel
                     float4* d4 = reinterpret_cast<float4*>(part_row + ((size_t)row * 2 + 1) * kD + half * 64 + cc * 32);
 #pragma unroll
@@ -785,11 +774,7 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
 #pragma unroll
             for (int hc = 0; hc < 2; ++hc) {
                 uint32_t v[64];
-                tmem_ld32(taddr + L::TM_DP + hc * 64, v);
-                tmem_ld32(taddr + L::TM_DP + hc * 64 + 32, v + 32);
-                tmem_ld_wait();
-                reg_fence32(v);
-                reg_fence32(v + 32);
+                tmem_ld64_sync(taddr + L::TM_DP + hc * 64, v);
                 if (hc == 1) {
                     tc_fence_before();
                     mbar_arrive(smem_u32(&bars.dq_drained));
@@ -811,9 +796,7 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 uint32_t o[32];
-                tmem_ld32(taddr + L::TM_DK + cc * 32, o);
-                tmem_ld_wait();
-                reg_fence32(o);
+                tmem_ld32_sync(taddr + L::TM_DK + cc * 32, o);
                 if (row_valid && part_row) {  // unscaled fp32 partial
                     float4* d4 = reinterpret_cast<float4*>(part_row + (size_t)row * 2 * kD + cc * 32);
 #pragma unroll

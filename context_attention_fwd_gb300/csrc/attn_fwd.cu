@@ -232,15 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             if (!(ok = mbar_wait(s_done, j & 1, wc))) break;
             tc_fence_after();
             uint32_t s[128];
-            tmem_ld32(taddr + s_cols + 0, s);
-            tmem_ld32(taddr + s_cols + 32, s + 32);
-            tmem_ld32(taddr + s_cols + 64, s + 64);
-            tmem_ld32(taddr + s_cols + 96, s + 96);
-            tmem_ld_wait();
-            reg_fence32(s);
-            reg_fence32(s + 32);
-            reg_fence32(s + 64);
-            reg_fence32(s + 96);
+            tmem_ld128_sync(taddr + s_cols, s);
             if (kv_len < kTile || diag) {
 #pragma unroll
                 for (int k = 0; k < 128; ++k)
@@ -291,9 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll
                 for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t o[32];
-                    tmem_ld32(taddr + o_cols + cc * 32, o);
-                    tmem_ld_wait();
-                    reg_fence32(o);
+                    tmem_ld32_sync(taddr + o_cols + cc * 32, o);
 #pragma unroll
                     for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
                     tmem_st32(taddr + o_cols + cc * 32, o);
@@ -338,9 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll
                 for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t o[32];
-                    tmem_ld32(taddr + o_cols + cc * 32, o);
-                    tmem_ld_wait();
-                    reg_fence32(o);
+                    tmem_ld32_sync(taddr + o_cols + cc * 32, o);
                     if (valid) {
                         float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D + cc * 32);
 #pragma unroll
@@ -366,9 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll
                 for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t o[32];
-                    tmem_ld32(taddr + o_cols + cc * 32, o);
-                    tmem_ld_wait();
-                    reg_fence32(o);
+                    tmem_ld32_sync(taddr + o_cols + cc * 32, o);
                     if (valid) {
                         uint4* dst = reinterpret_cast<uint4*>(dst_row + cc * 32);
 #pragma unroll

@@ -184,33 +184,59 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
                      "=r"(a[o + 4]), "=r"(a[o + 5]), "=r"(a[o + 6]), "=r"(a[o + 7])
 #define CTX_W8(a, o) "r"(a[o + 0]), "r"(a[o + 1]), "r"(a[o + 2]), "r"(a[o + 3]), \
                      "r"(a[o + 4]), "r"(a[o + 5]), "r"(a[o + 6]), "r"(a[o + 7])
-#define CTX_P8(a, o) "+r"(a[o + 0]), "+r"(a[o + 1]), "+r"(a[o + 2]), "+r"(a[o + 3]), \
-                     "+r"(a[o + 4]), "+r"(a[o + 5]), "+r"(a[o + 6]), "+r"(a[o + 7])
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+// TMEM -> registers, 32 lanes x N columns of 32 bits (lane = thread of the
+// warp), followed by tcgen05.wait::ld in the same asm statement.  tcgen05.ld
+// writes its destination registers asynchronously; with the wait inside the
+// statement the registers are only defined, as far as the compiler knows,
+// once the data is there, so it can neither read them (for a spill or a
+// move) nor reuse them before the load has landed.  Wider reads are issued
+// as consecutive x32 loads: one x64 or x128 load measured slower here.
+__device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t* r) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
+        "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
         : CTX_R8(r, 0), CTX_R8(r, 8), CTX_R8(r, 16), CTX_R8(r, 24)
-        : "r"(taddr));
+        : "r"(taddr)
+        : "memory");
 }
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+__device__ __forceinline__ void tmem_ld64_sync(uint32_t taddr, uint32_t* r) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : CTX_R8(r, 0), CTX_R8(r, 8)
-        : "r"(taddr));
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
+        "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
+        "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : CTX_R8(r, 0), CTX_R8(r, 8), CTX_R8(r, 16), CTX_R8(r, 24),
+          CTX_R8(r, 32), CTX_R8(r, 40), CTX_R8(r, 48), CTX_R8(r, 56)
+        : "r"(taddr + 0), "r"(taddr + 32)
+        : "memory");
 }
-__device__ __forceinline__ void tmem_ld_wait() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-// Pins registers after a wait::ld so no use of them is hoisted above the wait.
-__device__ __forceinline__ void reg_fence32(uint32_t* r) {
-    asm volatile("" : CTX_P8(r, 0), CTX_P8(r, 8), CTX_P8(r, 16), CTX_P8(r, 24));
-}
-__device__ __forceinline__ void reg_fence16(uint32_t* r) {
-    asm volatile("" : CTX_P8(r, 0), CTX_P8(r, 8));
+__device__ __forceinline__ void tmem_ld128_sync(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
+        "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%128];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
+        "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%129];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
+        "%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+        "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%130];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
+        "%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
+        "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%131];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : CTX_R8(r, 0), CTX_R8(r, 8), CTX_R8(r, 16), CTX_R8(r, 24),
+          CTX_R8(r, 32), CTX_R8(r, 40), CTX_R8(r, 48), CTX_R8(r, 56),
+          CTX_R8(r, 64), CTX_R8(r, 72), CTX_R8(r, 80), CTX_R8(r, 88),
+          CTX_R8(r, 96), CTX_R8(r, 104), CTX_R8(r, 112), CTX_R8(r, 120)
+        : "r"(taddr + 0), "r"(taddr + 32), "r"(taddr + 64), "r"(taddr + 96)
+        : "memory");
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
     asm volatile(
