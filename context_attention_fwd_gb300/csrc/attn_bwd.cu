@@ -58,7 +58,7 @@ struct BwdLayout {
     static constexpr uint32_t OFF_Q = OFF_V + TILE;          // 2 stages
     static constexpr uint32_t OFF_DO = OFF_Q + 2 * TILE;     // 2 stages
     static constexpr uint32_t OFF_DS = OFF_DO + 2 * TILE;
-    static constexpr uint32_t OFF_STAT = OFF_DS + DS_TILE;   // 2 stages x (lse2[128], delta[128])
+    static constexpr uint32_t OFF_STAT = OFF_DS + DS_TILE;   // 2 stages x (-lse2[128], delta[128])
     static constexpr uint32_t OFF_BARS = OFF_STAT + 2 * 1024;
     static constexpr uint32_t SMEM = OFF_BARS + 256;
     static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 384, TM_COLS = 512;
@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                 }
                 const size_t slot = ((size_t)(b * p.Hq + q.h) * ct.ntiles + q.t) * kTile;
                 const uint32_t sst = sbase + L::OFF_STAT + st * 1024;
-                bulk_load(sst, p.lse2 + slot, 512, qf);
+                bulk_load(sst, p.nlse2 + slot, 512, qf);
                 bulk_load(sst + 512, p.delta + slot, 512, qf);
                 last_ph[st] = ph;
             }
@@ -306,21 +306,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             const int q_start = q_first_row(q);
             const bool diag = p.causal && q.r == c && kv_start + kv_len - 1 > q_start;
             const int lo = diag ? kv_start + row - q_start - half * 64 : 0;  // mask columns k < lo
-            const float4* lse2 = reinterpret_cast<const float4*>(stat_base + st * 256 + half * 64);
+            const float4* nlse2 = reinterpret_cast<const float4*>(stat_base + st * 256 + half * 64);
             const float4* delta = reinterpret_cast<const float4*>(stat_base + st * 256 + 128 + half * 64);
             if (!(ok = mbar_wait(smem_u32(&bars.q_full[st]), ph, wc))) break;
             if (!(ok = mbar_wait(smem_u32(&bars.s_full), i & 1, wc))) break;
             tc_fence_after();
             uint32_t pr[64];
             tmem_ld64_sync(taddr + s_cols, pr);
-            // P^T (fp32 kept in pr); padded query columns have lse2 = +inf -> 0
+            // P^T (fp32 kept in pr); padded query columns have -lse2 = -inf -> 0
+            const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
-            for (int k4 = 0; k4 < 16; ++k4) {
-                const float4 l4 = lse2[k4];
-                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    pr[4 * k4 + e] = __float_as_uint(ex2(fmaf(__uint_as_float(pr[4 * k4 + e]), sc, -lv[e])));
+            for (int k4 = 0; k4 < 16; ++k4) {  // query columns in pairs: two-lane fp32 instructions
+                const float4 l4 = nlse2[k4];
+                const float2 x0 = ffma2(make_float2(__uint_as_float(pr[4 * k4]), __uint_as_float(pr[4 * k4 + 1])), sc2,
+                                        make_float2(l4.x, l4.y));
+                const float2 x1 = ffma2(make_float2(__uint_as_float(pr[4 * k4 + 2]), __uint_as_float(pr[4 * k4 + 3])),
+                                        sc2, make_float2(l4.z, l4.w));
+                pr[4 * k4 + 0] = __float_as_uint(ex2(x0.x));
+                pr[4 * k4 + 1] = __float_as_uint(ex2(x0.y));
+                pr[4 * k4 + 2] = __float_as_uint(ex2(x1.x));
+                pr[4 * k4 + 3] = __float_as_uint(ex2(x1.y));
             }
             if (diag || kv_len < kTile) {  // tile-uniform: only edge tiles pay for masking
                 const int lo_eff = row_valid ? lo : 64;  // zero columns k < lo_eff
@@ -352,12 +357,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                 for (int k4 = 0; k4 < 8; ++k4) {
                     const float4 d4 = delta[cc * 8 + k4];
                     const int q0 = cc * 32 + 4 * k4;
-                    const float a0 = __uint_as_float(pr[q0 + 0]) * (__uint_as_float(dp[4 * k4 + 0]) - d4.x);
-                    const float a1 = __uint_as_float(pr[q0 + 1]) * (__uint_as_float(dp[4 * k4 + 1]) - d4.y);
-                    const float a2 = __uint_as_float(pr[q0 + 2]) * (__uint_as_float(dp[4 * k4 + 2]) - d4.z);
-                    const float a3 = __uint_as_float(pr[q0 + 3]) * (__uint_as_float(dp[4 * k4 + 3]) - d4.w);
-                    w[2 * k4] = pack_bf16x2(a0, a1);
-                    w[2 * k4 + 1] = pack_bf16x2(a2, a3);
+                    const float2 a01 = fmul2(make_float2(__uint_as_float(pr[q0]), __uint_as_float(pr[q0 + 1])),
+                                             fsub2(make_float2(__uint_as_float(dp[4 * k4]), __uint_as_float(dp[4 * k4 + 1])),
+                                                   make_float2(d4.x, d4.y)));
+                    const float2 a23 = fmul2(make_float2(__uint_as_float(pr[q0 + 2]), __uint_as_float(pr[q0 + 3])),
+                                             fsub2(make_float2(__uint_as_float(dp[4 * k4 + 2]), __uint_as_float(dp[4 * k4 + 3])),
+                                                   make_float2(d4.z, d4.w)));
+                    w[2 * k4] = pack_bf16x2(a01.x, a01.y);
+                    w[2 * k4 + 1] = pack_bf16x2(a23.x, a23.y);
                 }
                 // 32 query columns = four 16-byte chunks of the 128-byte swizzled row
 #pragma unroll

@@ -282,13 +282,14 @@ __global__ void __launch_bounds__(kF256Threads, 1) attn_fwd256_kernel(const __gr
                 for (int k = 0; k < 128; ++k)
                     if (k >= lim) s[k] = __float_as_uint(-INFINITY);
             }
-            float mx8[8];
+            float mx8[8];  // eight running maxima, three-input max
 #pragma unroll
-            for (int e = 0; e < 8; ++e) mx8[e] = __uint_as_float(s[e]);
+            for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(__uint_as_float(s[e]), __uint_as_float(s[120 + e]));
 #pragma unroll
-            for (int k = 8; k < 128; k += 8)
+            for (int k = 8; k < 120; k += 16)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], __uint_as_float(s[k + e]));
+                for (int e = 0; e < 8; ++e)
+                    mx8[e] = fmax3(mx8[e], __uint_as_float(s[k + e]), __uint_as_float(s[k + 8 + e]));
             const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                    fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             if (first) {
@@ -307,19 +308,21 @@ __global__ void __launch_bounds__(kF256Threads, 1) attn_fwd256_kernel(const __gr
                 }
             }
             const float neg = m_ref == -INFINITY ? 0.f : -m_ref * sc;
-            float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            // columns in pairs (two-lane fp32 instructions); four running pair sums
+            const float2 sc2 = make_float2(sc, sc), neg2 = make_float2(neg, neg);
+            float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                              make_float2(0.f, 0.f)};
 #pragma unroll
             for (int k = 0; k < 64; ++k) {
-                const float p0 = ex2(fmaf(__uint_as_float(s[2 * k]), sc, neg));
-                const float p1 = ex2(fmaf(__uint_as_float(s[2 * k + 1]), sc, neg));
-                sum8[(2 * k) & 7] += p0;
-                sum8[(2 * k + 1) & 7] += p1;
-                s[k] = pack_bf16x2(p0, p1);
+                const float2 x = ffma2(make_float2(__uint_as_float(s[2 * k]), __uint_as_float(s[2 * k + 1])), sc2, neg2);
+                const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+                sum4[k & 3] = fadd2(sum4[k & 3], pp);
+                s[k] = pack_bf16x2(pp.x, pp.y);
             }
             tmem_st32(taddr + s_cols + 0, s);
             tmem_st32(taddr + s_cols + 32, s + 32);
-            const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                              ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+            const float sum = ((sum4[0].x + sum4[0].y) + (sum4[1].x + sum4[1].y)) +
+                              ((sum4[2].x + sum4[2].y) + (sum4[3].x + sum4[3].y));
             l = l * alpha + sum;
             if (__any_sync(0xffffffffu, rescale)) {
                 // O must hold PV(j-1) before it is rescaled.  At this point
@@ -404,7 +407,7 @@ struct B256 {
     static constexpr uint32_t OFF_K = 0;                          // resident K: 4 boxes
     static constexpr uint32_t OFF_RING = OFF_K + 4 * kBox;        // 64 KB
     static constexpr uint32_t OFF_DS = OFF_RING + SLOTS * kSlot;  // 192 KB
-    static constexpr uint32_t OFF_STAT = OFF_DS + DS_TILE;        // 2 stages x (lse2[128], delta[128])
+    static constexpr uint32_t OFF_STAT = OFF_DS + DS_TILE;        // 2 stages x (-lse2[128], delta[128])
     static constexpr uint32_t OFF_BARS = OFF_STAT + 2 * 1024;
     static constexpr uint32_t SMEM = OFF_BARS + 256;
     static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 384, TM_COLS = 512;
@@ -431,7 +434,7 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 
 // Ring loads of query tile i (column half h of this CTA), in this order:
 //   0: Q[:, other half]   1: V[:, other half]   2: dO[:, other half]
-//   3: Q[:, half h] (+ lse2, delta)   4: V[:, half h]   5: dO[:, half h]
+//   3: Q[:, half h] (+ -lse2, delta)   4: V[:, half h]   5: dO[:, half h]
 // Load n goes to slot n mod 4 and waits for the release of load n - 4; the
 // releases happen in the order S part A (0), dP part A (1, 2), dK (3),
 // dP part B (4), dV (5), so no load waits on a product that needs it.  Two
@@ -545,7 +548,7 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
                     if (k == 3) {
                         const size_t slot = ((size_t)(b * p.Hq + q.h) * ct.ntiles + q.t) * kTile;
                         const uint32_t sst = sbase + L::OFF_STAT + (i & 1) * 1024;
-                        bulk_load(sst, p.lse2 + slot, 512, f);
+                        bulk_load(sst, p.nlse2 + slot, 512, f);
                         bulk_load(sst + 512, p.delta + slot, 512, f);
                     }
                     last[slot_of(n)] = phase_of(n);
@@ -669,20 +672,25 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
             const int q_start = qw.first_row(q);
             const bool diag = p.causal && q.r == c && kv_start + kv_len - 1 > q_start;
             const int lo = diag ? kv_start + row - q_start - half * 64 : 0;
-            const float4* lse2 = reinterpret_cast<const float4*>(stat_base + (i & 1) * 256 + half * 64);
+            const float4* nlse2 = reinterpret_cast<const float4*>(stat_base + (i & 1) * 256 + half * 64);
             const float4* delta = reinterpret_cast<const float4*>(stat_base + (i & 1) * 256 + 128 + half * 64);
             if (!(ok = mbar_wait(full_bar(n3), phase_of(n3), wc))) break;
             if (!(ok = mbar_wait(smem_u32(&bars.s_full), i & 1, wc))) break;
             tc_fence_after();
             uint32_t pr[64];
             tmem_ld64_sync(taddr + s_cols, pr);
+            const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
-            for (int k4 = 0; k4 < 16; ++k4) {
-                const float4 l4 = lse2[k4];
-                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    pr[4 * k4 + e] = __float_as_uint(ex2(fmaf(__uint_as_float(pr[4 * k4 + e]), sc, -lv[e])));
+            for (int k4 = 0; k4 < 16; ++k4) {  // query columns in pairs: two-lane fp32 instructions
+                const float4 l4 = nlse2[k4];
+                const float2 x0 = ffma2(make_float2(__uint_as_float(pr[4 * k4]), __uint_as_float(pr[4 * k4 + 1])), sc2,
+                                        make_float2(l4.x, l4.y));
+                const float2 x1 = ffma2(make_float2(__uint_as_float(pr[4 * k4 + 2]), __uint_as_float(pr[4 * k4 + 3])),
+                                        sc2, make_float2(l4.z, l4.w));
+                pr[4 * k4 + 0] = __float_as_uint(ex2(x0.x));
+                pr[4 * k4 + 1] = __float_as_uint(ex2(x0.y));
+                pr[4 * k4 + 2] = __float_as_uint(ex2(x1.x));
+                pr[4 * k4 + 3] = __float_as_uint(ex2(x1.y));
             }
             if (diag || kv_len < kTile) {
                 const int lo_eff = row_valid ? lo : 64;
@@ -713,12 +721,14 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
                 for (int k4 = 0; k4 < 8; ++k4) {
                     const float4 d4 = delta[cc * 8 + k4];
                     const int qc = cc * 32 + 4 * k4;
-                    const float a0 = __uint_as_float(pr[qc + 0]) * (__uint_as_float(dp[4 * k4 + 0]) - d4.x);
-                    const float a1 = __uint_as_float(pr[qc + 1]) * (__uint_as_float(dp[4 * k4 + 1]) - d4.y);
-                    const float a2 = __uint_as_float(pr[qc + 2]) * (__uint_as_float(dp[4 * k4 + 2]) - d4.z);
-                    const float a3 = __uint_as_float(pr[qc + 3]) * (__uint_as_float(dp[4 * k4 + 3]) - d4.w);
-                    wv[2 * k4] = pack_bf16x2(a0, a1);
-                    wv[2 * k4 + 1] = pack_bf16x2(a2, a3);
+                    const float2 a01 = fmul2(make_float2(__uint_as_float(pr[qc]), __uint_as_float(pr[qc + 1])),
+                                             fsub2(make_float2(__uint_as_float(dp[4 * k4]), __uint_as_float(dp[4 * k4 + 1])),
+                                                   make_float2(d4.x, d4.y)));
+                    const float2 a23 = fmul2(make_float2(__uint_as_float(pr[qc + 2]), __uint_as_float(pr[qc + 3])),
+                                             fsub2(make_float2(__uint_as_float(dp[4 * k4 + 2]), __uint_as_float(dp[4 * k4 + 3])),
+                                                   make_float2(d4.z, d4.w)));
+                    wv[2 * k4] = pack_bf16x2(a01.x, a01.y);
+                    wv[2 * k4 + 1] = pack_bf16x2(a23.x, a23.y);
                 }
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {

@@ -266,8 +266,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int k = 0; k < 64; ++k) {
-                const float p0 = ex2(fmaf(__uint_as_float(s[2 * k]), sc, neg));
-                const float p1 = ex2(fmaf(__uint_as_float(s[2 * k + 1]), sc, neg));
+                float x0, x1;
+                if constexpr (D == 64) {
+                    // columns in pairs (one two-lane fp32 instruction): faster at
+                    // D = 64, slower at D = 128, where the kernel is at its
+                    // register limit and the pairs need aligned register pairs
+                    const float2 x = ffma2(make_float2(__uint_as_float(s[2 * k]), __uint_as_float(s[2 * k + 1])),
+                                           make_float2(sc, sc), make_float2(neg, neg));
+                    x0 = x.x;
+                    x1 = x.y;
+                } else {
+                    x0 = fmaf(__uint_as_float(s[2 * k]), sc, neg);
+                    x1 = fmaf(__uint_as_float(s[2 * k + 1]), sc, neg);
+                }
+                const float p0 = ex2(x0), p1 = ex2(x1);
                 sum8[(2 * k) & 7] += p0;
                 sum8[(2 * k + 1) & 7] += p1;
                 s[k] = pack_bf16x2(p0, p1);  // packed P overwrites scores already consumed

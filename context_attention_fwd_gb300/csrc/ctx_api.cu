@@ -220,15 +220,16 @@ __global__ void exchange_kernel(const uint16_t* __restrict__ x, uint16_t* __rest
 }
 
 // Row statistics for the backward, written in tile-major order
-// [B][Hq][ntiles][128]: delta = sum_d dO o O (fp32) and lse * log2(e).
-// Slots past a chunk's end get delta 0 and lse +inf, which makes their
-// probabilities exactly 0 in the backward kernel.  Each thread also zeroes
+// [B][Hq][ntiles][128]: delta = sum_d dO o O (fp32) and -lse * log2(e)
+// (negated, so the backward adds it in one fused multiply-add).  Slots past
+// a chunk's end get delta 0 and -inf, which makes their probabilities
+// exactly 0 in the backward kernel.  Each thread also zeroes
 // its 8 columns of the row's fp32 dQ accumulator (tile-major
 // [B][Hq][ntiles][D/4][128][4]), which the backward kernel adds into.
 __global__ void bwd_stats_kernel(const __nv_bfloat16* __restrict__ out, int64_t osb, int64_t oss,
                                  int64_t osh, const __nv_bfloat16* __restrict__ dout, int64_t dsb,
                                  int64_t dss, int64_t dsh, const float* __restrict__ lse,
-                                 float* __restrict__ lse2_t, float* __restrict__ delta_t,
+                                 float* __restrict__ nlse2_t, float* __restrict__ delta_t,
                                  float* __restrict__ dq_acc, const ChunkTable ct, int Hq, int S, int D,
                                  int64_t nslots) {
     const int tpr = D / 8;  // threads per row, 8 elements each
@@ -267,7 +268,7 @@ __global__ void bwd_stats_kernel(const __nv_bfloat16* __restrict__ out, int64_t 
     for (int w = tpr / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w, tpr);
     if (in_range && part == 0) {
         delta_t[slot] = valid ? acc : 0.f;
-        lse2_t[slot] = valid ? lse[((int64_t)b * Hq + h) * S + s] * 1.4426950408889634f : INFINITY;
+        nlse2_t[slot] = valid ? -(lse[((int64_t)b * Hq + h) * S + s] * 1.4426950408889634f) : -INFINITY;
     }
 }
 
@@ -690,7 +691,7 @@ int ctx_attn_bwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
         return CTX_ERR_WORKSPACE;
     const size_t slots = (size_t)B * Hq * p.ct.ntiles * kTile;
     char* ws = static_cast<char*>(workspace);
-    float* lse2_t = reinterpret_cast<float*>(ws);
+    float* nlse2_t = reinterpret_cast<float*>(ws);
     float* delta_t = reinterpret_cast<float*>(ws + align256(slots * 4));
     float* dq_acc = reinterpret_cast<float*>(ws + 2 * align256(slots * 4));
     int64_t bwd_ctas = 0;
@@ -708,7 +709,7 @@ int ctx_attn_bwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
     p.causal = causal ? 1 : 0;
     p.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
     p.scale_log2 = p.scale * 1.4426950408889634f;
-    p.lse2 = lse2_t;
+    p.nlse2 = nlse2_t;
     p.delta = delta_t;
     p.dq_acc = dq_acc;
     p.dk = static_cast<__nv_bfloat16*>(tdk.data);
@@ -732,7 +733,7 @@ int ctx_attn_bwd(const ctx_tensor_t* q, const ctx_tensor_t* k, const ctx_tensor_
         const int blk = 256;
         bwd_stats_kernel<<<(unsigned)((threads + blk - 1) / blk), blk, 0, s>>>(
             static_cast<const __nv_bfloat16*>(to.data), to.sb, to.ss, to.sh,
-            static_cast<const __nv_bfloat16*>(tdo.data), tdo.sb, tdo.ss, tdo.sh, lse, lse2_t,
+            static_cast<const __nv_bfloat16*>(tdo.data), tdo.sb, tdo.ss, tdo.sh, lse, nlse2_t,
             delta_t, dq_acc, p.ct, (int)Hq, (int)S, (int)D, (int64_t)slots);
         if ((rc = launch_status())) return rc;
     }

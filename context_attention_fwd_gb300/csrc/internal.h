@@ -94,7 +94,7 @@ struct BwdParams {
     int causal;
     float scale, scale_log2;
     // per-row statistics in tile-major order [B][Hq][ntiles][128]:
-    const float* lse2;   // lse * log2(e)
+    const float* nlse2;  // -lse * log2(e)
     const float* delta;  // rowsum(dO o O)
     // fp32 dQ accumulator, tile-major [B][Hq][ntiles][D/4][128][4], zeroed
     float* dq_acc;
