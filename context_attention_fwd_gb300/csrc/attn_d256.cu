@@ -454,11 +454,16 @@ __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __gr
     const uint32_t sK = sbase + L::OFF_K, sRing = sbase + L::OFF_RING, sDS = sbase + L::OFF_DS;
     const float* stat_base = reinterpret_cast<const float*>(smem + L::OFF_STAT);
     const int warp = warp_id(), lane = lane_id();
-    // z = 2 (b * hsplit + split) + column half
-    const GridPos gp = grid_pos<kHeadMajor>();
-    const unsigned z = gp.z;
-    const int kt = gp.tile, hk = gp.head, hh = z & 1;
-    const int b = (z >> 1) / p.hsplit, split = (z >> 1) % p.hsplit;
+    // Head-major grid (kv heads, 2 (b * hsplit + split) + column half, tiles);
+    // tile-major grid (2 tile + column half, kv heads, b * hsplit + split):
+    // there the two column halves of a KV tile are launched side by side and
+    // stream the same Q, dO and V tiles at the same time, so the second read
+    // of each tile hits in L2.
+    const int kt = kHeadMajor ? (int)blockIdx.z : (int)(blockIdx.x >> 1);
+    const int hk = kHeadMajor ? (int)blockIdx.x : (int)blockIdx.y;
+    const int hh = kHeadMajor ? (int)(blockIdx.y & 1) : (int)(blockIdx.x & 1);
+    const int zs = kHeadMajor ? (int)(blockIdx.y >> 1) : (int)blockIdx.z;  // b * hsplit + split
+    const int b = zs / p.hsplit, split = zs % p.hsplit;
     const ChunkTable& ct = p.ct;
     const int c = chunk_of_tile(ct, kt);
     const int kv_start = ct.off[c] + (kt - ct.tile_off[c]) * kTile;
@@ -855,8 +860,10 @@ int launch_attn_bwd256(const BwdParams& p, cudaStream_t s) {
             return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, B256::SMEM) == cudaSuccess;
         }))
         return 4;
-    // z = 2 (b * hsplit + split) + column half
-    kern<<<grid_dims(p.head_major, p.ct.ntiles, p.Hkv, p.B * 2 * p.hsplit), kB256Threads, B256::SMEM, s>>>(p);
+    // grid decode at the top of attn_bwd256_kernel
+    const dim3 grid = p.head_major ? dim3(p.Hkv, p.B * 2 * p.hsplit, p.ct.ntiles)
+                                   : dim3(2 * p.ct.ntiles, p.Hkv, p.B * p.hsplit);
+    kern<<<grid, kB256Threads, B256::SMEM, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
 
