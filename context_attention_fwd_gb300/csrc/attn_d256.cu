@@ -7,8 +7,9 @@
 //   * forward: one 128-row query tile per CTA; TMEM holds two score buffers
 //     (S_0, S_1: 128 columns each) and O (256 columns), so S(j+1) is computed
 //     while the softmax of tile j runs; two threads issue the products (S
-//     from one, PV from the other) so that both reach the tensor core at once.  K and V stream through a ring of
-//     32 KB slots: K(j) as two column halves (the two halves of the QK^T
+//     from one, PV from the other) so that both reach the tensor core at
+//     once.  K and V stream through a ring of 32 KB slots, loaded by two
+//     threads: K(j) as two column halves (the two halves of the QK^T
 //     contraction), V(j) as two 64-row halves (the two halves of the PV
 //     contraction, N = 256 each).
 //   * backward: dK and dV of one KV tile do not fit in TMEM together with
@@ -16,7 +17,9 @@
 //     by column half h of dK, dV and dQ.  Both recompute S^T and dP^T over
 //     the full 256-column contraction; TMEM is then S^T, dP^T (later dQ_h),
 //     dV_h, dK_h = 4 x 128 columns as in the D = 128 kernel.  K stays
-//     resident; Q, V and dO stream through a ring of 32 KB column-half slots.
+//     resident; Q, V and dO stream through a ring of 32 KB column-half slots
+//     loaded by two threads.  Warps 0..7 do the P / dS math, 8..11 drain dQ_h,
+//     12 and 15 load, 13 issues S^T and dP^T, 14 dV_h, dK_h and dQ_h.
 //     Short sequences give few KV tiles, so the query heads of a GQA group
 //     may further be split over hsplit CTAs, which then write fp32 partial
 //     dK/dV rows for a separate summing kernel.
