@@ -42,8 +42,8 @@ L2_NOTE = "inputs larger than L2 (q/k/v/dout 805 MB vs 126.5 MB L2); no flush"
 
 # dram traffic per launch of the backward kernel from one ncu capture (see
 # profiles/); valid only while the kernel source is the one it was taken on.
-NCU_BWD = {"bytes_per_launch": 1327076096 + 857917696,  # dram read + write, S=32760 H=24 D=128 P=8
-           "source_sha256": "7843320547229b9e74a9247ee56482a4f8d842c8c108fe7df2ec0cd34de69c3e"}
+NCU_BWD = {"bytes_per_launch": 1320996352 + 850899712,  # dram read + write, S=32760 H=24 D=128 P=8
+           "source_sha256": "2bcf66524566ddefaea9a26f4a35ec781a902d54c39579cef1259735577b8322"}
 
 
 # Dense bf16 tensor-core rate of one SM per clock: one M=128, N=128, K=16

@@ -102,6 +102,8 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 
 template <int D, bool kHeadMajor>
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
+    griddep_wait();  // the previous kernel in the stream is complete (launch_kernel)
+    griddep_launch_dependents();
     using L = BwdLayout<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
     BwdBars& bars = *reinterpret_cast<BwdBars*>(smem + L::OFF_BARS);
@@ -471,8 +473,9 @@ int launch_bwd_do(const BwdParams& p, cudaStream_t s) {
                                         L::SMEM) == cudaSuccess;
         }))
         return 4;
-    attn_bwd_kernel<D, kHeadMajor><<<grid_dims(kHeadMajor, p.ct.ntiles, p.Hkv, p.B), kThreads, L::SMEM, s>>>(p);
-    return cudaGetLastError() == cudaSuccess ? 0 : 4;
+    const cudaError_t e = launch_kernel(p.pdl != 0, attn_bwd_kernel<D, kHeadMajor>,
+                                        grid_dims(kHeadMajor, p.ct.ntiles, p.Hkv, p.B), dim3(kThreads), L::SMEM, s, p);
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
 
 template <int D>

@@ -82,6 +82,8 @@ constexpr float kRescaleThreshold = 8.0f;
 
 template <bool kPartials, bool kHeadMajor>
 __global__ void __launch_bounds__(kF256Threads, 1) attn_fwd256_kernel(const __grid_constant__ FwdParams p) {
+    griddep_wait();  // the previous kernel in the stream is complete (launch_kernel)
+    griddep_launch_dependents();
     using L = F256;
     extern __shared__ uint8_t smem_raw[];
     __shared__ F256Bars bars;
@@ -450,6 +452,8 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 // per reader), whichever thread then refills it.
 template <bool kHeadMajor>
 __global__ void __launch_bounds__(kB256Threads, 1) attn_bwd256_kernel(const __grid_constant__ BwdParams p) {
+    griddep_wait();  // the previous kernel in the stream is complete (launch_kernel)
+    griddep_launch_dependents();
     using L = B256;
     extern __shared__ __align__(1024) uint8_t smem[];
     B256Bars& bars = *reinterpret_cast<B256Bars*>(smem + L::OFF_BARS);
@@ -852,8 +856,9 @@ int launch_attn_fwd256(const FwdParams& p, cudaStream_t s) {
             return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, F256::SMEM) == cudaSuccess;
         }))
         return 4;
-    kern<<<grid_dims(p.head_major, p.ct.ntiles, p.Hq, p.B), kF256Threads, F256::SMEM, s>>>(p);
-    return cudaGetLastError() == cudaSuccess ? 0 : 4;
+    const cudaError_t e = launch_kernel(p.pdl != 0, kern, grid_dims(p.head_major, p.ct.ntiles, p.Hq, p.B),
+                                        dim3(kF256Threads), F256::SMEM, s, p);
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
 
 int launch_attn_bwd256(const BwdParams& p, cudaStream_t s) {
@@ -866,8 +871,8 @@ int launch_attn_bwd256(const BwdParams& p, cudaStream_t s) {
     // grid decode at the top of attn_bwd256_kernel
     const dim3 grid = p.head_major ? dim3(p.Hkv, p.B * 2 * p.hsplit, p.ct.ntiles)
                                    : dim3(2 * p.ct.ntiles, p.Hkv, p.B * p.hsplit);
-    kern<<<grid, kB256Threads, B256::SMEM, s>>>(p);
-    return cudaGetLastError() == cudaSuccess ? 0 : 4;
+    const cudaError_t e = launch_kernel(p.pdl != 0, kern, grid, dim3(kB256Threads), B256::SMEM, s, p);
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
 
 }  // namespace ctxattn

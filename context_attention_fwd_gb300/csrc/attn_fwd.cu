@@ -91,6 +91,8 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
 
 template <int D, bool kPartials, bool kHeadMajor>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
+    griddep_wait();  // the previous kernel in the stream is complete (launch_kernel)
+    griddep_launch_dependents();
     using L = FwdLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ FwdBars bars;
@@ -404,9 +406,9 @@ int launch_fwd_dpo(const FwdParams& p, cudaStream_t s) {
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) == cudaSuccess;
         }))
         return 4;
-    attn_fwd_kernel<D, kPartials, kHeadMajor>
-        <<<grid_dims(kHeadMajor, p.ct.npairs, p.Hq, p.B), kThreads, L::SMEM, s>>>(p);
-    return cudaGetLastError() == cudaSuccess ? 0 : 4;
+    const cudaError_t e = launch_kernel(p.pdl != 0, attn_fwd_kernel<D, kPartials, kHeadMajor>,
+                                        grid_dims(kHeadMajor, p.ct.npairs, p.Hq, p.B), dim3(kThreads), L::SMEM, s, p);
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
 
 template <int D, bool kPartials>

@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <utility>
 
 #include "tmap.h"
 
@@ -34,6 +35,26 @@ __host__ __device__ inline int debug_skip_step(int debug, int n) {
 // A set-up that is done once per device (a kernel's shared-memory limit is
 // an attribute of the function on each device; setting it on every launch
 // costs host time).  f() returns true on success.
+// Launches a kernel of the attention calls.  With pdl set it uses
+// programmatic stream serialization: the kernel may be scheduled while the
+// previous kernel in the stream finishes, and waits for it (griddep_wait in
+// ptx.cuh) before touching global memory.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t s, Args&&... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 struct OncePerDevice {
     std::atomic<uint64_t> done{0};
     template <typename F>
@@ -85,6 +106,7 @@ struct FwdParams {
     uint64_t timeout_ns;
     int head_major;  // launch order of the attention kernel (grid_pos in walk.cuh)
     int debug;       // kDebug* bits (0 in normal use)
+    int pdl;         // launch with programmatic stream serialization (launch_kernel)
 };
 
 struct BwdParams {
@@ -111,6 +133,7 @@ struct BwdParams {
     uint64_t timeout_ns;
     int head_major;  // launch order of the attention kernel (grid_pos in walk.cuh)
     int debug;       // kDebug* bits (0 in normal use)
+    int pdl;         // launch with programmatic stream serialization (launch_kernel)
 };
 
 int launch_attn_fwd(const FwdParams& p, int D, cudaStream_t s);

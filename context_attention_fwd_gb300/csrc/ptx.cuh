@@ -86,6 +86,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
     return mbar_wait_slow(bar, parity, w);
 }
 
+// ------------------------------------------------------------------ launch order
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may be scheduled while the previous kernel in its stream is
+// still running.  griddep_wait blocks until that kernel has completed and
+// its memory operations are visible (without the launch attribute it
+// returns at once).  Every kernel of the attention calls executes it before
+// its first global memory access, so each also completes only after its
+// predecessor: the memory effects keep the stream's order, and only the
+// launch and the prologue overlap the previous kernel's tail.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Allows the next kernel in the stream to be scheduled once every CTA of
+// this grid has issued it (or exited); its CTAs then wait in griddep_wait.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
