@@ -27,6 +27,12 @@
  *    device status word).  The library caches per-device addresses of its
  *    own device variables; they are invalid after cudaDeviceReset, so reload
  *    the library after a reset.
+ *  - Short attention calls (about 1024 tokens and less) launch their kernels
+ *    with programmatic stream serialization when the stream is not being
+ *    captured: a kernel may be scheduled while the previous kernel in the
+ *    stream finishes, but it waits for that kernel to complete before it
+ *    reads or writes any memory, so the stream's order of memory effects is
+ *    unchanged for the caller's own work before and after a call.
  *  - Diagnostics: CTX_ATTN_LOG=1 in the environment prints one line per
  *    attention call to stderr (chunks, tiles, CTAs, kernel variant, launch
  *    order); every entry point that launches work opens an NVTX range named
